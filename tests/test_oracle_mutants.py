@@ -1,0 +1,81 @@
+"""The oracle's pins must catch plausible mistakes in the oracle itself.
+
+Each case below plants one mistake (a dropped term, an off-by-one index, a
+wrong comparison, a lost bit) in a temporary copy of ``oracle/fsdp_oracle.c``,
+builds it, swaps it in for the real oracle library, and re-runs the pins of
+tests/test_oracle_pins.py.  At least one pin must fail for every mutant.
+Everything runs on the CPU; the mistakes are planted in the oracle only.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "pack: source index off by one":
+        ("int64_t j = (int64_t)r * chunk[p] + i;\n          int64_t d",
+         "int64_t j = (int64_t)r * chunk[p] + i + (i > 0);\n          int64_t d"),
+    "pack: last real element treated as padding":
+        ("if (j < numel[p])\n            cast_element(grads[p]",
+         "if (j + 1 < numel[p])\n            cast_element(grads[p]"),
+    "pack: padding filled with wrapped values":
+        ("else\n            store_zero(bufs[b], bucket_dtype[b], d);",
+         "else\n            cast_element(grads[p], grad_dtype[p], j % numel[p], bufs[b], bucket_dtype[b], d);"),
+    "pack: bucket offset dropped":
+        ("(int64_t)r * bucket_S[b] + bucket_off[p] + i;",
+         "(int64_t)r * bucket_S[b] + i;"),
+    "pack: rank stride uses chunk instead of row length":
+        ("(int64_t)r * bucket_S[b] + bucket_off[p] + i;",
+         "(int64_t)r * chunk[p] + bucket_off[p] + i;"),
+    "rne: ties always round down":
+        ("if (d_lo < d_hi) return toward_zero;", "if (d_lo <= d_hi) return toward_zero;"),
+    "rne: ties to odd":
+        ("return (toward_zero & 1) ? away : toward_zero;", "return (toward_zero & 1) ? toward_zero : away;"),
+    "rne: NaN not quieted":
+        ("return (uint16_t)((u >> 16) | 0x0040);", "return (uint16_t)(u >> 16);"),
+    "rne: subnormal scale wrong":
+        ("mag = ldexp((double)f, -126 - 7);", "mag = ldexp((double)f, -127 - 7);"),
+    "bf16 decode: exponent bias wrong":
+        ("mag = ldexp(128.0 + (double)f, e - 127 - 7);", "mag = ldexp(128.0 + (double)f, e - 126 - 7);"),
+    "copy-in: element offset in group dropped":
+        ("cast_element(shards[p], shard_dtype[p], i, base, param_dtype[p],\n                     group_elem_off[p] + i);",
+         "cast_element(shards[p], shard_dtype[p], i, base, param_dtype[p],\n                     i);"),
+    "copy-in: gap bytes not cleared":
+        ("memset(ag_in, 0, (size_t)S_ag);", "memset(ag_in, 0xAB, (size_t)S_ag);"),
+    "copy-out: group start dropped":
+        ("(int64_t)r * S_ag + group_byte_off[group_of[p]] +", "(int64_t)r * S_ag +"),
+    "copy-out: rank rows transposed":
+        ("int64_t j = (int64_t)r * chunk[p] + i;\n        if (j >= numel[p]) continue;",
+         "int64_t j = (int64_t)(W - 1 - r) * chunk[p] + i;\n        if (j >= numel[p]) continue;"),
+}
+
+PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and callable(getattr(pins, n))]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name!r} not found exactly once"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(lib), str(path), "-lm"],
+                   check=True)
+    saved = oracle._load()
+    oracle._lib = oracle._bind(ctypes.CDLL(os.fspath(lib)))
+    failed = []
+    try:
+        for pin in PINS:
+            try:
+                pin()
+            except AssertionError:
+                failed.append(pin.__name__)
+                break
+    finally:
+        oracle._lib = saved
+    assert failed, f"no pin caught mutant {name!r}"

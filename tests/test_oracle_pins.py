@@ -1,0 +1,452 @@
+"""Pins for the CPU oracle: it is checked against what the pages and the
+mathematics fix, never against itself or the CUDA path.
+
+* values the pages print ("The unit you wrapped": the Linear(4, 4) shard and
+  gradient shards, the 36 / 18 / 9 per-rank counts, the Linear(3, 3) padding;
+  the news item's 192 MiB figure);
+* brute force: the definitions restated with numpy pad / reshape / hstack and
+  byte appends, and torch's own dtype conversions as the cast;
+* rounding: a textbook FP32 -> BF16 table, torch's CPU conversion on a large
+  structured sample, and an exact-rational (fractions.Fraction) rounding
+  reference written by quantum scaling and Python's ties-to-even round();
+* invariants (padding slots are zero, total sizes, roundtrip).
+
+Every test here runs without a GPU.  The functions take no fixtures so that
+tests/test_oracle_mutants.py can re-run them against deliberately broken
+copies of the oracle.
+"""
+import itertools
+import random
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import BF16, F32, Param, plan
+from fsdp2_gradient_packing_gb300 import workloads as wl
+from golden_io import f32_bits, records, sections
+
+NP = {F32: np.uint32, BF16: np.uint16}
+
+
+# ---------------------------------------------------------------------------
+# Independent helpers: torch's conversions, numpy layout restatements.
+# ---------------------------------------------------------------------------
+def torch_cast(bits: np.ndarray, src: int, dst: int) -> np.ndarray:
+    bits = np.ascontiguousarray(bits)
+    if src == dst:
+        return bits.copy()
+    if src == BF16:
+        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        return t.to(torch.float32).numpy().view(np.uint32).copy()
+    t = torch.from_numpy(bits.view(np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def first_appearance(keys):
+    seen = []
+    for k in keys:
+        if k not in seen:
+            seen.append(k)
+    return seen
+
+
+def brute_pack(params, W, grads):
+    """Pad each flat gradient to a multiple of W, view it as W rows, cast, and
+    lay the rows of every parameter of a bucket side by side."""
+    outs = []
+    for rd in first_appearance([p.reduce_dtype for p in params]):
+        blocks = []
+        for p, g in zip(params, grads):
+            if p.reduce_dtype != rd:
+                continue
+            c = -(-p.numel // W)
+            v = np.pad(torch_cast(g, p.grad_dtype, rd), (0, c * W - p.numel))
+            blocks.append(v.reshape(W, c))
+        outs.append(np.hstack(blocks).reshape(-1))
+    return outs
+
+
+def brute_copy_in(params, shards):
+    """Append each (shard dtype, param dtype) group's cast shards as bytes,
+    zero-padding to a 16-byte boundary before each group and at the end.
+    Returns the bytes and each parameter's byte position."""
+    out = bytearray()
+    where = {}
+    for pair in first_appearance([(p.shard_dtype, p.param_dtype) for p in params]):
+        out += bytes((-len(out)) % 16)
+        for k, (p, s) in enumerate(zip(params, shards)):
+            if (p.shard_dtype, p.param_dtype) == pair:
+                where[k] = len(out)
+                out += torch_cast(s, p.shard_dtype, p.param_dtype).tobytes()
+    out += bytes((-len(out)) % 16)
+    return np.frombuffer(bytes(out), np.uint8).copy(), where
+
+
+def brute_copy_out(params, W, gathered, where):
+    rows = gathered.reshape(W, -1)
+    outs = []
+    for k, p in enumerate(params):
+        c = -(-p.numel // W)
+        sz = 4 if p.param_dtype == F32 else 2
+        parts = [rows[r, where[k]:where[k] + c * sz].view(NP[p.param_dtype]) for r in range(W)]
+        full = np.concatenate(parts) if parts else np.zeros(0, NP[p.param_dtype])
+        outs.append(full[:p.numel])
+    return outs
+
+
+def rand_bits(rng, n, dt):
+    x = rng.standard_normal(n).astype(np.float32).view(np.uint32)
+    return x if dt == F32 else (x >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Page pins.
+# ---------------------------------------------------------------------------
+def test_linear4x4_rank0_holds_rows_0_and_1():
+    g = sections("linear4x4_w2.txt")
+    shard = f32_bits(g["rank0_shard"])
+    weight = np.zeros((4, 4), np.float32)
+    weight[0] = np.float32(np.array(g["weight_row0"], dtype=np.float64))
+    weight[1] = np.float32(np.array(g["weight_row1"], dtype=np.float64))
+    weight[2:] = np.random.default_rng(3).standard_normal((2, 4)).astype(np.float32)
+    pl = plan([Param(16)], 2)
+    assert pl.chunk == [8] and pl.bucket_S == [8]
+    buf, = oracle.pack_reduce_scatter(pl, [weight.view(np.uint32).reshape(-1)])
+    assert np.array_equal(buf[:8], shard)                     # rank 0 = rows 0-1
+    assert np.array_equal(buf[8:], weight[2:].view(np.uint32).reshape(-1))
+    # Gathering the unit gives the (4, 4) parameter back on every rank.
+    rows = [oracle.allgather_copy_in(pl, [buf[r * 8:(r + 1) * 8]]) for r in range(2)]
+    full, = oracle.allgather_copy_out(pl, np.concatenate(rows))
+    shape = tuple(int(v) for v in g["summoned_shape"])
+    assert np.array_equal(full.reshape(shape), weight.view(np.uint32))
+
+
+def test_linear4x4_grad_shards():
+    g = sections("linear4x4_w2.txt")
+    grad = np.zeros((4, 4), np.float32)
+    grad[1] = np.float32(1.2830595970)
+    pl = plan([Param(16)], 2)
+    buf, = oracle.pack_reduce_scatter(pl, [grad.view(np.uint32).reshape(-1)])
+    assert np.array_equal(buf[:8], f32_bits(g["rank0_grad_shard"]))
+    assert np.array_equal(buf[8:], f32_bits(g["rank1_grad_shard"]))
+
+
+def test_wrap_policy_per_rank_counts():
+    for rec in records("wrap_policy_counts.txt"):
+        choice, W, counts = rec[0], int(rec[1]), [int(v) for v in rec[2:]]
+        grouping = {"no_policy": "model", "block_units": "block", "linear_units": "linear"}[choice]
+        work = wl.tiny_two_blocks(W=W, grouping=grouping)
+        assert sum(p.numel for g in work.groups for p in g) == 144
+        got = []
+        for g in work.groups:
+            pl = plan(oracle.params_from_specs(g), W)
+            assert len(pl.bucket_S) == 1                      # one reduce dtype
+            assert pl.bucket_S[0] == sum(pl.group_elems)      # same count gathered
+            got.append(pl.bucket_S[0])
+        assert got == counts, (choice, got, counts)
+
+
+def test_linear3x3_padding():
+    d = {r[0]: r[1:] for r in records("linear3x3_w4_padding.txt")}
+    n, W = int(d["numel"][0]), int(d["world_size"][0])
+    pl = plan([Param(n)], W)
+    assert [pl.chunk[0]] * W == [int(v) for v in d["shard"]]
+    assert pl.chunk[0] * W == int(d["padded_total"][0])
+    grad = (np.arange(1, n + 1, dtype=np.float32)).view(np.uint32)
+    buf, = oracle.pack_reduce_scatter(pl, [grad])
+    pad = buf[n:]
+    assert pad.size == int(d["padding"][0]) and np.all(pad == 0)
+    assert np.array_equal(buf[:n], grad)
+
+
+def test_isolated_pack_avoided_temporary_is_192_mib():
+    d = {r[0]: r[1:] for r in records("isolated_pack_test.txt")}
+    work = wl.mixed_50m(W=8)
+    params = oracle.params_from_specs(work.groups[0])
+    n_bf16 = sum(p.numel for p in params if p.grad_dtype == BF16)
+    n_all = sum(p.numel for p in params)
+    assert n_bf16 == 50_331_648
+    assert round(n_all / 1e6, 1) == float(d["elements_millions"][0])
+    assert n_bf16 * 4 == int(d["avoided_temporary_mib"][0]) * 2**20   # FP32 copy of the BF16 grads
+    pl = plan(params, 8)
+    assert pl.bucket_S == [6_292_480] and len(pl.bucket_dtype) == 1
+    assert 8 * pl.bucket_S[0] * 4 == 201_359_360
+
+
+def test_one_bucket_per_reduce_dtype_in_first_appearance_order():
+    same = [Param(5, BF16, F32), Param(7, F32, F32), Param(3, BF16, F32)]
+    assert plan(same, 4).bucket_dtype == [F32]
+    mixed = [Param(5, BF16, BF16), Param(7, F32, F32), Param(3, BF16, BF16)]
+    pl = plan(mixed, 4)
+    assert pl.bucket_dtype == [BF16, F32]
+    assert pl.bucket_of == [0, 1, 0] and pl.bucket_off == [0, 0, 2]
+    assert pl.bucket_S == [3, 2]
+
+
+def test_one_allgather_input_with_groups_by_dtype_pair():
+    params = [Param(10, shard_dtype=F32, param_dtype=BF16), Param(3, shard_dtype=F32, param_dtype=F32),
+              Param(7, shard_dtype=F32, param_dtype=BF16), Param(1, shard_dtype=BF16, param_dtype=BF16)]
+    pl = plan(params, 2)
+    assert pl.group_pair == [(F32, BF16), (F32, F32), (BF16, BF16)]
+    assert pl.chunk == [5, 2, 4, 1]
+    assert pl.group_of == [0, 1, 0, 2] and pl.group_elem_off == [0, 0, 5, 0]
+    # group 0: 9 BF16 = 18 B -> group 1 at 32, 2 FP32 = 8 B -> group 2 at 48, 1 BF16 -> 64
+    assert pl.group_byte_off == [0, 32, 48] and pl.S_ag == 64
+
+
+def test_empty_layout_and_empty_parameters():
+    pl = plan([], 4)
+    assert pl.bucket_dtype == [] and pl.group_pair == [] and pl.S_ag == 0
+    assert oracle.pack_reduce_scatter(pl, []) == []
+    assert oracle.allgather_copy_in(pl, []).size == 0
+    pl = plan([Param(0, BF16, BF16), Param(0)], 3)
+    assert pl.chunk == [0, 0] and pl.bucket_S == [0, 0] and pl.S_ag == 0
+    bufs = oracle.pack_reduce_scatter(pl, [np.zeros(0, np.uint16), np.zeros(0, np.uint32)])
+    assert [b.size for b in bufs] == [0, 0]
+
+
+def test_world_size_one_is_plain_concatenation():
+    rng = np.random.default_rng(11)
+    params = [Param(5, BF16, F32), Param(3, F32, F32), Param(4, F32, BF16)]
+    grads = [rand_bits(rng, p.numel, p.grad_dtype) for p in params]
+    pl = plan(params, 1)
+    assert pl.chunk == [5, 3, 4]
+    f32buf, bf16buf = oracle.pack_reduce_scatter(pl, grads)
+    assert np.array_equal(f32buf, np.concatenate([torch_cast(grads[0], BF16, F32), grads[1]]))
+    assert np.array_equal(bf16buf, torch_cast(grads[2], F32, BF16))
+
+
+# ---------------------------------------------------------------------------
+# Brute force on tiny layouts.
+# ---------------------------------------------------------------------------
+def _pack_case(params, W, seed):
+    rng = np.random.default_rng(seed)
+    grads = [rand_bits(rng, p.numel, p.grad_dtype) for p in params]
+    got = oracle.pack_reduce_scatter(plan(params, W), grads)
+    want = brute_pack(params, W, grads)
+    assert len(got) == len(want)
+    for a, b in zip(got, want):
+        assert a.dtype == b.dtype and np.array_equal(a, b), (params, W)
+
+
+def _gather_case(params, W, seed):
+    rng = np.random.default_rng(seed)
+    pl = plan(params, W)
+    shards = [[rand_bits(rng, c, p.shard_dtype) for p, c in zip(params, pl.chunk)] for _ in range(W)]
+    rows = []
+    for r in range(W):
+        got = oracle.allgather_copy_in(pl, shards[r])
+        want, where = brute_copy_in(params, shards[r])
+        assert np.array_equal(got, want), (params, W, r)
+        rows.append(got)
+    gathered = np.concatenate(rows)
+    got = oracle.allgather_copy_out(pl, gathered)
+    want = brute_copy_out(params, W, gathered, where)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b), (params, W)
+
+
+def test_brute_force_pack_one_and_two_params_exhaustive():
+    dts = (F32, BF16)
+    for W in range(1, 6):
+        for n in range(14):
+            for gd, rd in itertools.product(dts, dts):
+                _pack_case([Param(n, gd, rd)], W, seed=n * 7 + W)
+    k = 0
+    for W in range(1, 6):
+        for n1, n2 in itertools.product(range(14), range(14)):
+            for g1, r1, g2, r2 in itertools.product(dts, dts, dts, dts):
+                _pack_case([Param(n1, g1, r1), Param(n2, g2, r2)], W, seed=k)
+                k += 1
+
+
+def test_brute_force_pack_three_params_sampled():
+    rnd = random.Random(5)
+    dts = (F32, BF16)
+    for k in range(1500):
+        W = rnd.randint(1, 5)
+        params = [Param(rnd.randint(0, 13), rnd.choice(dts), rnd.choice(dts)) for _ in range(3)]
+        _pack_case(params, W, seed=10_000 + k)
+
+
+def test_brute_force_copy_in_out_one_and_two_params_exhaustive():
+    dts = (F32, BF16)
+    for W in range(1, 6):
+        for n in range(14):
+            for sd, pd in itertools.product(dts, dts):
+                _gather_case([Param(n, shard_dtype=sd, param_dtype=pd)], W, seed=n + 100 * W)
+    k = 0
+    rnd = random.Random(9)
+    for W in range(1, 6):
+        for n1, n2 in itertools.product(range(14), range(14)):
+            s1, p1, s2, p2 = (rnd.choice(dts) for _ in range(4))
+            _gather_case([Param(n1, shard_dtype=s1, param_dtype=p1),
+                          Param(n2, shard_dtype=s2, param_dtype=p2)], W, seed=k)
+            k += 1
+
+
+def test_brute_force_copy_in_out_three_params_sampled():
+    rnd = random.Random(6)
+    dts = (F32, BF16)
+    for k in range(600):
+        W = rnd.randint(1, 5)
+        params = [Param(rnd.randint(0, 13), shard_dtype=rnd.choice(dts), param_dtype=rnd.choice(dts))
+                  for _ in range(3)]
+        _gather_case(params, W, seed=20_000 + k)
+
+
+def test_pack_samples_match_whole_pack():
+    rng = np.random.default_rng(21)
+    params = [Param(37, BF16, F32), Param(5, F32, BF16), Param(64, F32, F32), Param(3, BF16, BF16)]
+    grads = [rand_bits(rng, p.numel, p.grad_dtype) for p in params]
+    pl = plan(params, 8)
+    whole = oracle.pack_reduce_scatter(pl, grads)
+    for b, buf in enumerate(whole):
+        idx = np.arange(buf.size)
+        assert np.array_equal(oracle.pack_samples(pl, grads, b, idx), buf)
+
+
+# ---------------------------------------------------------------------------
+# Invariants.
+# ---------------------------------------------------------------------------
+def test_padding_slots_are_zero_and_sizes_add_up():
+    rnd = random.Random(17)
+    dts = (F32, BF16)
+    for k in range(300):
+        W = rnd.choice([1, 2, 3, 4, 8, 64])
+        params = [Param(rnd.randint(0, 200), rnd.choice(dts), rnd.choice(dts)) for _ in range(rnd.randint(1, 5))]
+        pl = plan(params, W)
+        total = sum(W * S for S in pl.bucket_S)
+        n = sum(p.numel for p in params)
+        assert total >= n
+        assert (total == n) == all(p.numel % W == 0 for p in params)
+        # gradients with no zero bits anywhere: every zero in the buffer is padding
+        grads = [np.full(p.numel, 0x3F80 if p.grad_dtype == BF16 else 0x3F800000, NP[p.grad_dtype])
+                 for p in params]
+        bufs = oracle.pack_reduce_scatter(pl, grads)
+        assert sum(int(np.count_nonzero(b == 0)) for b in bufs) == total - n
+
+
+def test_roundtrip_copy_in_then_copy_out_reproduces_parameters():
+    rnd = random.Random(23)
+    rng = np.random.default_rng(23)
+    dts = (F32, BF16)
+    for k in range(200):
+        W = rnd.choice([1, 2, 3, 4, 8])
+        params = [Param(rnd.randint(0, 100), shard_dtype=rnd.choice(dts), param_dtype=rnd.choice(dts))
+                  for _ in range(rnd.randint(1, 4))]
+        pl = plan(params, W)
+        # full parameters whose values are representable in every dtype
+        full = [torch_cast(rand_bits(rng, p.numel, BF16), BF16, p.shard_dtype) for p in params]
+        rows = []
+        for r in range(W):
+            shards = []
+            for p, c, x in zip(params, pl.chunk, full):
+                padded = np.pad(x, (0, c * W - p.numel))
+                shards.append(padded.reshape(W, c)[r].copy())
+            rows.append(oracle.allgather_copy_in(pl, shards))
+        got = oracle.allgather_copy_out(pl, np.concatenate(rows))
+        for p, x, y in zip(params, full, got):
+            assert np.array_equal(y, torch_cast(x, p.shard_dtype, p.param_dtype))
+            assert np.array_equal(torch_cast(y, p.param_dtype, p.shard_dtype), x)
+
+
+# ---------------------------------------------------------------------------
+# Number formats.
+# ---------------------------------------------------------------------------
+RNE_TABLE = [  # (FP32 bits, BF16 bits): IEEE-754 round to nearest, ties to even
+    (0x3F800000, 0x3F80),   # 1.0 exact
+    (0x3F808000, 0x3F80),   # 1 + 2^-8: tie, 0x3F80 is even
+    (0x3F818000, 0x3F82),   # 1 + 3*2^-8: tie, 0x3F82 is even
+    (0x3F808001, 0x3F81),   # just above the tie
+    (0x3F807FFF, 0x3F80),   # just below the tie
+    (0xBF808000, 0xBF80),   # negative tie
+    (0xBF818000, 0xBF82),
+    (0x7F7FC99E, 0x7F80),   # 3.4e38 rounds past the largest BF16 to +inf
+    (0x7F7FFFFF, 0x7F80),   # FLT_MAX -> +inf
+    (0x7F7F8000, 0x7F80),   # tie between BF16 max and 2^128 -> inf (even)
+    (0x7F7F7FFF, 0x7F7F),   # below that tie stays finite
+    (0xFF7FFFFF, 0xFF80),
+    (0x000116C2, 0x0001),   # 1e-40, subnormal: nearest is 0x0001
+    (0x00000001, 0x0000),   # smallest subnormal rounds to +0
+    (0x80000001, 0x8000),   # ... and to -0 when negative
+    (0x00008000, 0x0000),   # tie between 0 and 0x0001 -> even (0)
+    (0x00018000, 0x0002),   # tie between 0x0001 and 0x0002 -> even
+    (0x00008001, 0x0001),
+    (0x007FFFFF, 0x0080),   # largest subnormal rounds up to the smallest normal
+    (0x00000000, 0x0000), (0x80000000, 0x8000),
+    (0x7F800000, 0x7F80), (0xFF800000, 0xFF80),
+]
+
+
+def test_rne_textbook_table():
+    got = oracle.f32_to_bf16(np.array([a for a, _ in RNE_TABLE], np.uint32))
+    assert [int(v) for v in got] == [b for _, b in RNE_TABLE]
+
+
+def test_rne_matches_torch_on_structured_and_random_patterns():
+    hi = np.arange(1 << 16, dtype=np.uint32) << np.uint32(16)
+    lows = np.array([0x0000, 0x0001, 0x3FFF, 0x4000, 0x7FFF, 0x8000, 0x8001, 0xC000, 0xFFFF], np.uint32)
+    x = (hi[:, None] | lows[None, :]).reshape(-1)
+    x = np.concatenate([x, np.random.default_rng(31).integers(0, 1 << 32, 1 << 22, dtype=np.uint64).astype(np.uint32)])
+    finite = (x & 0x7F800000) != 0x7F800000
+    inf = (x & 0x7FFFFFFF) == 0x7F800000
+    keep = finite | inf
+    assert np.array_equal(oracle.f32_to_bf16(x[keep]), torch_cast(x[keep], F32, BF16))
+
+
+def _exact_rne(u: int) -> int:
+    """Round the exact value of FP32 pattern u to BF16 by scaling to the BF16
+    quantum of its binade and rounding with Python's ties-to-even round()."""
+    x = Fraction(*np.uint32(u).view(np.float32).item().as_integer_ratio())
+    if x == 0:
+        return (u >> 16) & 0x8000
+    e = max(-126, abs(x).numerator.bit_length() - abs(x).denominator.bit_length())
+    while Fraction(2) ** e > abs(x):
+        e -= 1
+    while Fraction(2) ** (e + 1) <= abs(x):
+        e += 1
+    e = max(-126, e)
+    q = Fraction(2) ** (e - 7)
+    y = round(x / q) * q
+    if abs(y) >= Fraction(2) ** 128:
+        return 0xFF80 if x < 0 else 0x7F80
+    f = np.float32(float(y))                # exact: y is a BF16 value
+    bits = int(f.view(np.uint32))
+    assert bits & 0xFFFF == 0
+    if y == 0:
+        bits = 0x80000000 if x < 0 else 0
+    return bits >> 16
+
+
+def test_rne_matches_exact_rational_rounding():
+    rng = np.random.default_rng(37)
+    x = rng.integers(0, 1 << 32, 6000, dtype=np.uint64).astype(np.uint32)
+    ties = (x & np.uint32(0xFFFF0000)) | np.uint32(0x8000)
+    sub = x & np.uint32(0x807FFFFF)                # subnormals
+    cases = np.concatenate([x, ties, sub, np.array([a for a, _ in RNE_TABLE], np.uint32)])
+    cases = cases[(cases & 0x7F800000) != 0x7F800000]
+    got = oracle.f32_to_bf16(cases)
+    for u, g in zip(cases.tolist(), got.tolist()):
+        assert g == _exact_rne(u), hex(u)
+
+
+def test_nan_keeps_sign_and_payload_and_is_quiet():
+    rng = np.random.default_rng(41)
+    mant = rng.integers(1, 1 << 23, 20000, dtype=np.uint64).astype(np.uint32)
+    sign = rng.integers(0, 2, 20000, dtype=np.uint64).astype(np.uint32) << np.uint32(31)
+    x = sign | np.uint32(0x7F800000) | mant
+    got = oracle.f32_to_bf16(x).astype(np.uint32)
+    assert np.all((got & 0x7F80) == 0x7F80) and np.all(got & 0x0040)
+    assert np.array_equal(got >> 15, x >> 31)
+    assert np.array_equal(got & 0x3F, (x >> 16) & 0x3F)
+
+
+def test_bf16_to_f32_exact_for_every_pattern():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.bf16_to_f32(h)
+    nan = ((h & 0x7F80) == 0x7F80) & ((h & 0x7F) != 0)
+    assert np.array_equal(got[~nan], torch_cast(h[~nan], BF16, F32))
+    assert np.array_equal(got[nan], h[nan].astype(np.uint32) << np.uint32(16))
