@@ -1,0 +1,563 @@
+// sm_103a kernels and the launching entry points of the C ABI.
+//
+// All three operations (reduce-scatter copy-in, all-gather copy-in, all-gather
+// copy-out) are "walk a table of contiguous runs and copy each one with a
+// cast": dst[k] = k < n_copy ? cast(src[k]) : +0 for k < n_total.  The host
+// planner (plan.cpp) emits the runs once per layout, cut into work items of at
+// most kStageBytes of source; one launch per call walks them.
+//
+// The work is bound by HBM bandwidth, so the kernel is a warp-specialised
+// pipeline built to keep many bytes in flight per SM with few registers and
+// to write only full, aligned 16-byte vectors:
+//   * warp 0, lane 0 is the producer.  For each item of its CTA it copies the
+//     16-byte-aligned interior of the item's source bytes into one stage of a
+//     shared-memory ring with one TMA bulk copy (cp.async.bulk), completion
+//     counted on that stage's "full" mbarrier;
+//   * warps 1..8 are consumers.  For each item they wait on the stage, then
+//     write the destination as 16-byte vectors: each lane reads the source
+//     bytes of one vector from shared memory at whatever byte phase they have
+//     (word loads plus a funnel shift), converts them and stores one aligned
+//     16-byte vector, so every warp store covers 512 contiguous bytes.  Vectors
+//     made only of padding are stored as zeros without reading anything.
+//     The few elements outside the staged interior (a run's ragged ends, and
+//     the destination's head before its first 16-byte boundary) are read and
+//     written one by one straight from global memory;
+//   * consumers release the stage on its "empty" mbarrier; the producer
+//     reuses it kStages items later.
+// FP32 -> BF16 rounding is done on the bits (round to nearest, ties to even),
+// so results do not depend on the device's FP modes.
+//
+// Every mbarrier wait is bounded (a limit in nanoseconds of %globaltimer).  A
+// wait that gives up sets a bit in the layout's device status word and the
+// thread leaves; the producer first waits (again bounded) for the bulk copies
+// it issued, so no copy is in flight when its CTA exits.  fsdp_sync_status()
+// reads and clears that word.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "layout.h"
+
+namespace fsdp {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kStages = 4;
+// Each stage holds kStageBytes plus 16 bytes of slack: the funnel read of the
+// last vector may touch one word past the staged bytes.
+constexpr int kStageStride = (int)kStageBytes + 16;
+constexpr int kSmemBytes = kStages * kStageStride + 2 * kStages * 8;
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+// Status bits written by a kernel whose bounded wait gave up.
+constexpr uint32_t kStatusConsumerWait = 1u;
+constexpr uint32_t kStatusProducerWait = 2u;
+constexpr uint32_t kStatusDrainWait = 4u;
+constexpr uint32_t kStatusBadItem = 8u;
+
+// Test hook: the producer of CTA 0 does not arm its first stage, so that
+// stage's consumers time out (no fault, no hang: every wait is bounded).
+constexpr int32_t kFaultSkipFirstStage = 1;
+
+// Per-call pointers travel by value in the parameter block: `slot` is read
+// with a run-time index, which __grid_constant__ allows without a local copy.
+template <int NSLOT>
+struct LaunchArgs {
+  const WorkItem *items;
+  int64_t n_items;
+  uint32_t *status;
+  uint64_t wait_limit_ns;
+  int32_t fault;
+  int32_t reserved;
+  const void *slot[NSLOT];
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, bulk copy, timer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete, for at most limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// One TMA bulk copy global -> shared, completion counted on `bar` in bytes.
+// Both addresses are 16-byte aligned and `bytes` is a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                              uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Element conversions on raw bits.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bf16_to_f32_bits(uint32_t h) { return h << 16; }
+
+// IEEE-754 round to nearest, ties to even, from binary32 to bfloat16 (the
+// upper 16 bits).  Adding 0x7FFF plus the lowest kept bit carries into the
+// kept half exactly when the dropped half is above one half ulp, or equal to
+// it with an odd kept half; a carry out of the largest finite value gives
+// infinity, as IEEE-754 requires.  NaN keeps its sign and upper payload and
+// gets the quiet bit.
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(uint32_t u) {
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x0040u;
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+template <int KIND>
+struct Traits;
+template <>
+struct Traits<KIND_F32_F32> {
+  using S = uint32_t;
+  using D = uint32_t;
+};
+template <>
+struct Traits<KIND_BF16_F32> {
+  using S = uint16_t;
+  using D = uint32_t;
+};
+template <>
+struct Traits<KIND_F32_BF16> {
+  using S = uint32_t;
+  using D = uint16_t;
+};
+template <>
+struct Traits<KIND_BF16_BF16> {
+  using S = uint16_t;
+  using D = uint16_t;
+};
+
+template <int KIND>
+__device__ __forceinline__ uint32_t convert_one(uint32_t x) {
+  if constexpr (KIND == KIND_BF16_F32) return bf16_to_f32_bits(x);
+  else if constexpr (KIND == KIND_F32_BF16) return f32_to_bf16_bits(x);
+  else return x;
+}
+
+template <int KIND>
+__device__ __forceinline__ void scalar_elem(const char *src, char *dst, int k, int n_copy) {
+  using S = typename Traits<KIND>::S;
+  using D = typename Traits<KIND>::D;
+  uint32_t v = 0;
+  if (k < n_copy) v = convert_one<KIND>((uint32_t)reinterpret_cast<const S *>(src)[k]);
+  reinterpret_cast<D *>(dst)[k] = (D)v;
+}
+
+// Source interior of an item that is staged in shared memory: bytes
+// [lo, hi) counted from the item's first source byte, where lo is the first
+// 16-byte boundary (or the end, for a run too short to have one) and hi - lo
+// is the largest multiple of 16 that fits.
+struct Interior {
+  int lo, hi;
+};
+
+__device__ __forceinline__ Interior interior_of(const char *src, int src_bytes) {
+  const int lead = (int)((16u - ((uint32_t)(uintptr_t)src & 15u)) & 15u);
+  Interior in;
+  in.lo = lead < src_bytes ? lead : src_bytes;
+  in.hi = in.lo + ((src_bytes - in.lo) & ~15);
+  return in;
+}
+
+// Consumer side of one item.  `stage` holds the item's interior.  `ct` is the
+// consumer thread index in [0, kConsumers).
+template <int KIND>
+__device__ __forceinline__ void consume_item(const WorkItem &w, const void *src_base, void *dst_base,
+                                             const uint8_t *stage, int ct) {
+  using S = typename Traits<KIND>::S;
+  using D = typename Traits<KIND>::D;
+  constexpr int DU = 16 / (int)sizeof(D);      // elements per destination vector
+  constexpr int SW = DU * (int)sizeof(S) / 4;  // source words per vector (2, 4 or 8)
+  const char *src = reinterpret_cast<const char *>(src_base) + w.src_off * (int64_t)sizeof(S);
+  char *dst = reinterpret_cast<char *>(dst_base) + w.dst_off * (int64_t)sizeof(D);
+  const int n_total = w.n_total, n_copy = w.n_copy;
+  const Interior in = interior_of(src, n_copy * (int)sizeof(S));
+
+  // Destination: scalar head to the first 16-byte boundary, vectors, tail.
+  int h = (int)(((16u - ((uint32_t)(uintptr_t)dst & 15u)) & 15u) / sizeof(D));
+  h = h < n_total ? h : n_total;
+  const int nvec = (n_total - h) / DU;
+  const int tail0 = h + nvec * DU;
+  if (ct < h) scalar_elem<KIND>(src, dst, ct, n_copy);
+  if (tail0 + ct < n_total) scalar_elem<KIND>(src, dst, tail0 + ct, n_copy);
+
+  const uint32_t *stage32 = reinterpret_cast<const uint32_t *>(stage);
+  for (int j = ct; j < nvec; j += kConsumers) {
+    const int e0 = h + j * DU;
+    uint4 *d = reinterpret_cast<uint4 *>(dst + e0 * (int)sizeof(D));
+    if (e0 >= n_copy) {
+      *d = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const int s_lo = e0 * (int)sizeof(S);
+    if (e0 + DU <= n_copy && s_lo >= in.lo && s_lo + DU * (int)sizeof(S) <= in.hi) {
+      const int off = s_lo - in.lo;  // byte offset inside the stage (even)
+      const int wi = off >> 2;
+      const int rb = (off & 3) * 8;
+      uint32_t wv[SW + 1], s[SW];
+#pragma unroll
+      for (int k = 0; k <= SW; ++k) wv[k] = stage32[wi + k];
+#pragma unroll
+      for (int k = 0; k < SW; ++k) s[k] = __funnelshift_r(wv[k], wv[k + 1], rb);
+      uint32_t o[4];
+      if constexpr (KIND == KIND_BF16_F32) {
+        o[0] = s[0] << 16;
+        o[1] = s[0] & 0xFFFF0000u;
+        o[2] = s[1] << 16;
+        o[3] = s[1] & 0xFFFF0000u;
+      } else if constexpr (KIND == KIND_F32_BF16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16_bits(s[2 * i]) | (f32_to_bf16_bits(s[2 * i + 1]) << 16);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = s[i];
+      }
+      *d = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll 1
+      for (int e = 0; e < DU; ++e) scalar_elem<KIND>(src, dst, e0 + e, n_copy);
+    }
+  }
+}
+
+template <int NSLOT>
+__global__ void __launch_bounds__(kThreads) walk_kernel(const __grid_constant__ LaunchArgs<NSLOT> a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageStride);
+  uint64_t *empty = full + kStages;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  if (warp == 0) {
+    if (lane != 0) return;
+    // Producer.
+    int64_t k = 0;
+    bool skipped_first = false;
+    for (int64_t i = blockIdx.x; i < a.n_items; i += gridDim.x, ++k) {
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
+        atomicOr(a.status, kStatusProducerWait);
+        break;
+      }
+      if (k == 0 && blockIdx.x == 0 && (a.fault & kFaultSkipFirstStage)) {
+        skipped_first = true;
+        continue;
+      }
+      const WorkItem w = a.items[i];
+      const int sz = (w.kind & 1) ? 2 : 4;
+      const char *src = reinterpret_cast<const char *>(a.slot[w.src_slot]) + w.src_off * (int64_t)sz;
+      const Interior in = interior_of(src, w.n_copy * sz);
+      uint32_t bytes = (uint32_t)(in.hi - in.lo);
+      if (bytes > (uint32_t)kStageBytes) {  // never planned; consumers skip such an item
+        atomicOr(a.status, kStatusBadItem);
+        bytes = 0;
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      if (bytes) bulk_copy_g2s(smem + s * kStageStride, src + in.lo, bytes, &full[s]);
+    }
+    // Leave no bulk copy in flight when this thread exits: wait for the last
+    // armed phase of every stage (consumers may have left early).
+    for (int64_t kk = k > kStages ? k - kStages : 0; kk < k; ++kk) {
+      if (kk == 0 && skipped_first) continue;
+      if (!mbar_wait(&full[kk % kStages], (uint32_t)(kk / kStages) & 1u, a.wait_limit_ns))
+        atomicOr(a.status, kStatusDrainWait);
+    }
+    return;
+  }
+
+  // Consumers.
+  const int ct = (int)threadIdx.x - 32;
+  int64_t k = 0;
+  for (int64_t i = blockIdx.x; i < a.n_items; i += gridDim.x, ++k) {
+    const int s = (int)(k % kStages);
+    if (!mbar_wait(&full[s], (uint32_t)(k / kStages) & 1u, a.wait_limit_ns)) {
+      if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
+      return;
+    }
+    const WorkItem w = a.items[i];
+    const void *sp = a.slot[w.src_slot];
+    {
+      // The producer refuses an item whose interior exceeds a stage; skip it too.
+      const int sz = (w.kind & 1) ? 2 : 4;
+      const Interior in = interior_of(reinterpret_cast<const char *>(sp) + w.src_off * (int64_t)sz, w.n_copy * sz);
+      if (in.hi - in.lo > (int)kStageBytes) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      }
+    }
+    void *dp = const_cast<void *>(a.slot[w.dst_slot]);
+    const uint8_t *stage = smem + s * kStageStride;
+    switch (w.kind) {
+      case KIND_F32_F32: consume_item<KIND_F32_F32>(w, sp, dp, stage, ct); break;
+      case KIND_BF16_F32: consume_item<KIND_BF16_F32>(w, sp, dp, stage, ct); break;
+      case KIND_F32_BF16: consume_item<KIND_F32_BF16>(w, sp, dp, stage, ct); break;
+      default: consume_item<KIND_BF16_BF16>(w, sp, dp, stage, ct); break;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+// Slot capacities of the three kernel variants.  The largest keeps the
+// parameter block under CUDA's 32,764-byte limit.
+constexpr int kSlotsSmall = 64;
+constexpr int kSlotsMedium = 512;
+constexpr int kSlotsLarge = FSDP_MAX_PARAMS + 2;
+static_assert(sizeof(LaunchArgs<kSlotsLarge>) <= 32764, "parameter block too large");
+
+std::atomic<int32_t> g_fault{0};
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+template <int NSLOT>
+fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptrs, int n_ptrs,
+                             cudaStream_t stream) {
+  LaunchArgs<NSLOT> a;
+  a.items = L->d_items + L->op[op].first;
+  a.n_items = L->op[op].count;
+  a.status = L->d_status;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  a.fault = g_fault.load(std::memory_order_relaxed);
+  a.reserved = 0;
+  for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
+  for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
+  void *args[] = {&a};
+  cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void *>(&walk_kernel<NSLOT>),
+                                   dim3((unsigned)L->op[op].grid), dim3(kThreads), args, kSmemBytes, stream);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  clear_error();
+  return FSDP_OK;
+}
+
+fsdp_status_t launch(const fsdp_layout *L, Op op, const void *const *ptrs, int n_ptrs, cudaStream_t stream) {
+  if (L->op[op].count == 0) {
+    clear_error();
+    return FSDP_OK;
+  }
+  if (n_ptrs <= kSlotsSmall) return launch_variant<kSlotsSmall>(L, op, ptrs, n_ptrs, stream);
+  if (n_ptrs <= kSlotsMedium) return launch_variant<kSlotsMedium>(L, op, ptrs, n_ptrs, stream);
+  return launch_variant<kSlotsLarge>(L, op, ptrs, n_ptrs, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Host-side argument checks (nothing is launched unless all pass).
+// ---------------------------------------------------------------------------
+fsdp_status_t check_layout(const fsdp_layout *L) {
+  if (!L) return fail(FSDP_EINVAL, "layout is NULL");
+  if (L->device < 0) return fail(FSDP_EINVAL, "layout was planned without a device table");
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (cur != L->device)
+    return fail(FSDP_EINVAL, "current device " + std::to_string(cur) + " is not the layout's device " +
+                                 std::to_string(L->device));
+  return FSDP_OK;
+}
+
+fsdp_status_t check_ptr(const void *p, int64_t bytes, int64_t align, const char *what, int64_t index) {
+  if (bytes == 0) return FSDP_OK;
+  std::string name = std::string(what) + (index >= 0 ? "[" + std::to_string(index) + "]" : "");
+  if (!p) return fail(FSDP_EINVAL, name + " is NULL");
+  if (((uintptr_t)p) % (uintptr_t)align)
+    return fail(FSDP_EINVAL, name + " is not " + std::to_string(align) + "-byte aligned");
+  return FSDP_OK;
+}
+
+template <int NSLOT>
+cudaError_t allow_smem() {
+  return cudaFuncSetAttribute(reinterpret_cast<const void *>(&walk_kernel<NSLOT>),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+}  // namespace
+
+fsdp_status_t device_setup(fsdp_layout *L) {
+  int dev = -1, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = allow_smem<kSlotsSmall>();
+  if (e == cudaSuccess) e = allow_smem<kSlotsMedium>();
+  if (e == cudaSuccess) e = allow_smem<kSlotsLarge>();
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<kSlotsSmall>, kThreads, kSmemBytes);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("device query failed: ") + cudaGetErrorString(e));
+  const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  for (int op = 0; op < OP_COUNT; ++op) {
+    int64_t g = L->op[op].count < resident ? L->op[op].count : resident;
+    L->op[op].grid = (int32_t)(g > 0 ? g : 0);
+  }
+  // One allocation: the status word (padded to 32 bytes), then the work table.
+  const size_t table_bytes = L->items.size() * sizeof(WorkItem);
+  void *mem = nullptr;
+  e = cudaMalloc(&mem, 32 + table_bytes);
+  if (e != cudaSuccess)
+    return fail(FSDP_ENOMEM, std::string("cudaMalloc of the work table: ") + cudaGetErrorString(e));
+  L->d_status = reinterpret_cast<uint32_t *>(mem);
+  L->d_items = reinterpret_cast<WorkItem *>(reinterpret_cast<char *>(mem) + 32);
+  e = cudaMemset(mem, 0, 32);
+  if (e == cudaSuccess && table_bytes)
+    e = cudaMemcpy(L->d_items, L->items.data(), table_bytes, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(mem);
+    L->d_status = nullptr;
+    L->d_items = nullptr;
+    return fail(FSDP_ECUDA, std::string("work table upload: ") + cudaGetErrorString(e));
+  }
+  L->device = dev;
+  return FSDP_OK;
+}
+
+void device_release(fsdp_layout *L) {
+  if (!L->d_status) return;
+  int cur = -1;
+  const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != L->device;
+  if (switched) cudaSetDevice(L->device);
+  cudaFree(L->d_status);
+  if (switched) cudaSetDevice(cur);
+  L->d_status = nullptr;
+  L->d_items = nullptr;
+}
+
+}  // namespace fsdp
+
+using namespace fsdp;
+
+extern "C" {
+
+fsdp_status_t fsdp_pack_reduce_scatter(const fsdp_layout_t *L, const void *const *grads,
+                                       void *const *bucket_bufs, fsdp_stream_t stream) {
+  fsdp_status_t st = check_layout(L);
+  if (st != FSDP_OK) return st;
+  const int P = (int)L->desc.size(), B = (int)L->bucket.size();
+  if (P > 0 && !grads) return fail(FSDP_EINVAL, "grads is NULL");
+  if (B > 0 && !bucket_bufs) return fail(FSDP_EINVAL, "bucket_bufs is NULL");
+  for (int p = 0; p < P; ++p) {
+    const int64_t sz = dtype_bytes(L->desc[p].grad_dtype);
+    if ((st = check_ptr(grads[p], L->desc[p].numel * sz, sz, "grads", p)) != FSDP_OK) return st;
+  }
+  for (int b = 0; b < B; ++b) {
+    const int64_t sz = dtype_bytes(L->bucket[b].dtype);
+    if ((st = check_ptr(bucket_bufs[b], (int64_t)L->W * L->bucket[b].S * sz, sz, "bucket_bufs", b)) != FSDP_OK)
+      return st;
+  }
+  const void *ptrs[kSlotsLarge];
+  for (int p = 0; p < P; ++p) ptrs[p] = grads[p];
+  for (int b = 0; b < B; ++b) ptrs[P + b] = bucket_bufs[b];
+  return launch(L, OP_PACK, ptrs, P + B, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_allgather_copy_in(const fsdp_layout_t *L, const void *const *local_shards, void *ag_input,
+                                     fsdp_stream_t stream) {
+  fsdp_status_t st = check_layout(L);
+  if (st != FSDP_OK) return st;
+  const int P = (int)L->desc.size();
+  if (P > 0 && !local_shards) return fail(FSDP_EINVAL, "local_shards is NULL");
+  for (int p = 0; p < P; ++p) {
+    const int64_t sz = dtype_bytes(L->desc[p].shard_dtype);
+    if ((st = check_ptr(local_shards[p], L->param[p].chunk * sz, sz, "local_shards", p)) != FSDP_OK) return st;
+  }
+  if ((st = check_ptr(ag_input, L->S_ag, 16, "ag_input", -1)) != FSDP_OK) return st;
+  const void *ptrs[kSlotsLarge];
+  for (int p = 0; p < P; ++p) ptrs[p] = local_shards[p];
+  ptrs[P] = ag_input;
+  return launch(L, OP_COPY_IN, ptrs, P + 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_output, void *const *full_params,
+                                      fsdp_stream_t stream) {
+  fsdp_status_t st = check_layout(L);
+  if (st != FSDP_OK) return st;
+  const int P = (int)L->desc.size();
+  if ((st = check_ptr(ag_output, (int64_t)L->W * L->S_ag, 16, "ag_output", -1)) != FSDP_OK) return st;
+  if (P > 0 && !full_params) return fail(FSDP_EINVAL, "full_params is NULL");
+  for (int p = 0; p < P; ++p) {
+    const int64_t sz = dtype_bytes(L->desc[p].param_dtype);
+    if ((st = check_ptr(full_params[p], L->desc[p].numel * sz, sz, "full_params", p)) != FSDP_OK) return st;
+  }
+  const void *ptrs[kSlotsLarge];
+  ptrs[0] = ag_output;
+  for (int p = 0; p < P; ++p) ptrs[1 + p] = full_params[p];
+  return launch(L, OP_COPY_OUT, ptrs, P + 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream) {
+  fsdp_status_t st = check_layout(L);
+  if (st != FSDP_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  uint32_t word = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&word, L->d_status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word) e = cudaMemset(L->d_status, 0, sizeof(word));
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("status read: ") + cudaGetErrorString(e));
+  if (word)
+    return fail(FSDP_ETIMEOUT, "a bounded device wait gave up (status bits " + std::to_string(word) + ")");
+  clear_error();
+  return FSDP_OK;
+}
+
+void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns) {
+  g_fault.store(fault, std::memory_order_relaxed);
+  g_wait_limit_ns.store(wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kDefaultWaitLimitNs,
+                        std::memory_order_relaxed);
+}
+
+}  // extern "C"

@@ -1,0 +1,241 @@
+"""Thin ctypes binding of the C ABI in include/fsdp_pack.h.
+
+Each function here has the name of the C entry point it calls and only
+marshals arguments: tensors become device pointers (``data_ptr()``), the
+stream becomes a ``cudaStream_t`` handle, and a non-OK status becomes an
+``FsdpError``.  All packing work runs in the library's CUDA kernels; there is
+no fallback path.  Importing this module fails if the library has not been
+built (``__graft_entry__.build()`` or ``python -m
+fsdp2_gradient_packing_gb300._build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+if not os.path.exists(_build.LIB):
+    raise ImportError(
+        f"{_build.LIB} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(_build.LIB)
+
+FSDP_DTYPE_F32 = 0
+FSDP_DTYPE_BF16 = 1
+DTYPE_CODES = {"f32": FSDP_DTYPE_F32, "bf16": FSDP_DTYPE_BF16}
+DTYPE_BYTES = {FSDP_DTYPE_F32: 4, FSDP_DTYPE_BF16: 2}
+
+FSDP_OK, FSDP_EINVAL, FSDP_ENOMEM, FSDP_ECUDA, FSDP_EUNSUPPORTED, FSDP_ETIMEOUT = range(6)
+FSDP_MAX_PARAMS = 4000
+
+
+class fsdp_param_desc_t(ctypes.Structure):
+    _fields_ = [("numel", ctypes.c_int64), ("grad_dtype", ctypes.c_int32),
+                ("reduce_dtype", ctypes.c_int32), ("shard_dtype", ctypes.c_int32),
+                ("param_dtype", ctypes.c_int32)]
+
+
+class fsdp_layout_info_t(ctypes.Structure):
+    _fields_ = [("world_size", ctypes.c_int32), ("n_params", ctypes.c_int32),
+                ("n_buckets", ctypes.c_int32), ("n_groups", ctypes.c_int32),
+                ("ag_bytes", ctypes.c_int64), ("total_numel", ctypes.c_int64),
+                ("device", ctypes.c_int32), ("has_device_table", ctypes.c_int32),
+                ("pack_items", ctypes.c_int64), ("copy_in_items", ctypes.c_int64),
+                ("copy_out_items", ctypes.c_int64)]
+
+
+class fsdp_param_info_t(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int64), ("bucket", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("bucket_offset", ctypes.c_int64), ("group_offset", ctypes.c_int64),
+                ("ag_byte_offset", ctypes.c_int64)]
+
+
+class fsdp_bucket_info_t(ctypes.Structure):
+    _fields_ = [("reduce_dtype", ctypes.c_int32), ("n_params", ctypes.c_int32),
+                ("row_elems", ctypes.c_int64), ("bytes", ctypes.c_int64)]
+
+
+class fsdp_group_info_t(ctypes.Structure):
+    _fields_ = [("shard_dtype", ctypes.c_int32), ("param_dtype", ctypes.c_int32),
+                ("n_params", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("byte_offset", ctypes.c_int64), ("elems", ctypes.c_int64),
+                ("bytes", ctypes.c_int64)]
+
+
+_P = ctypes.c_void_p
+_ST = ctypes.c_int
+_LAYOUT = ctypes.c_void_p
+_SIGNATURES = {
+    "fsdp_plan_layout": (_ST, [ctypes.POINTER(fsdp_param_desc_t), ctypes.c_int32, ctypes.c_int32,
+                               ctypes.POINTER(_LAYOUT)]),
+    "fsdp_plan_layout_host": (_ST, [ctypes.POINTER(fsdp_param_desc_t), ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.POINTER(_LAYOUT)]),
+    "fsdp_layout_query": (_ST, [_LAYOUT, ctypes.POINTER(fsdp_layout_info_t)]),
+    "fsdp_layout_param": (_ST, [_LAYOUT, ctypes.c_int32, ctypes.POINTER(fsdp_param_info_t)]),
+    "fsdp_layout_bucket": (_ST, [_LAYOUT, ctypes.c_int32, ctypes.POINTER(fsdp_bucket_info_t)]),
+    "fsdp_layout_group": (_ST, [_LAYOUT, ctypes.c_int32, ctypes.POINTER(fsdp_group_info_t)]),
+    "fsdp_pack_reduce_scatter": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "fsdp_allgather_copy_in": (_ST, [_LAYOUT, ctypes.POINTER(_P), _P, _P]),
+    "fsdp_allgather_copy_out": (_ST, [_LAYOUT, _P, ctypes.POINTER(_P), _P]),
+    "fsdp_sync_status": (_ST, [_LAYOUT, _P]),
+    "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
+    "fsdp_layout_destroy": (None, [_LAYOUT]),
+    "fsdp_status_string": (ctypes.c_char_p, [_ST]),
+    "fsdp_last_error": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class FsdpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.fsdp_last_error().decode()
+        super().__init__(f"{where}: {fsdp_status_string(status)}" + (f" ({msg})" if msg else ""))
+
+
+def _check(status: int, where: str) -> None:
+    if status != FSDP_OK:
+        raise FsdpError(status, where)
+
+
+def fsdp_status_string(status: int) -> str:
+    return _lib.fsdp_status_string(status).decode()
+
+
+def fsdp_last_error() -> str:
+    return _lib.fsdp_last_error().decode()
+
+
+class Layout:
+    """Owner of an ``fsdp_layout_t *``; destroyed on ``close()`` or collection."""
+
+    def __init__(self, handle: int, n_params: int):
+        self.handle = handle
+        self.n_params = n_params
+
+    def close(self) -> None:
+        if self.handle:
+            _lib.fsdp_layout_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def _descs(params):
+    """Descriptors from fsdp_param_desc_t, (numel, g, rho, sigma, pi) tuples, or specs
+    with numel and dtype-string attributes (workloads.ParamSpec)."""
+    arr = (fsdp_param_desc_t * max(1, len(params)))()
+    for k, p in enumerate(params):
+        if isinstance(p, fsdp_param_desc_t):
+            arr[k] = p
+        elif isinstance(p, tuple):
+            arr[k] = fsdp_param_desc_t(*p)
+        else:
+            arr[k] = fsdp_param_desc_t(p.numel, DTYPE_CODES[p.grad_dtype], DTYPE_CODES[p.reduce_dtype],
+                                       DTYPE_CODES[p.shard_dtype], DTYPE_CODES[p.param_dtype])
+    return arr
+
+
+def fsdp_plan_layout(params, world_size: int) -> Layout:
+    arr = _descs(params)
+    out = _LAYOUT()
+    _check(_lib.fsdp_plan_layout(arr, len(params), world_size, ctypes.byref(out)), "fsdp_plan_layout")
+    return Layout(out.value, len(params))
+
+
+def fsdp_plan_layout_host(params, world_size: int) -> Layout:
+    arr = _descs(params)
+    out = _LAYOUT()
+    _check(_lib.fsdp_plan_layout_host(arr, len(params), world_size, ctypes.byref(out)),
+           "fsdp_plan_layout_host")
+    return Layout(out.value, len(params))
+
+
+def fsdp_layout_query(layout: Layout) -> fsdp_layout_info_t:
+    info = fsdp_layout_info_t()
+    _check(_lib.fsdp_layout_query(layout.handle, ctypes.byref(info)), "fsdp_layout_query")
+    return info
+
+
+def fsdp_layout_param(layout: Layout, p: int) -> fsdp_param_info_t:
+    info = fsdp_param_info_t()
+    _check(_lib.fsdp_layout_param(layout.handle, p, ctypes.byref(info)), "fsdp_layout_param")
+    return info
+
+
+def fsdp_layout_bucket(layout: Layout, b: int) -> fsdp_bucket_info_t:
+    info = fsdp_bucket_info_t()
+    _check(_lib.fsdp_layout_bucket(layout.handle, b, ctypes.byref(info)), "fsdp_layout_bucket")
+    return info
+
+
+def fsdp_layout_group(layout: Layout, g: int) -> fsdp_group_info_t:
+    info = fsdp_group_info_t()
+    _check(_lib.fsdp_layout_group(layout.handle, g, ctypes.byref(info)), "fsdp_layout_group")
+    return info
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _ptr_array(ts):
+    arr = (_P * max(1, len(ts)))()
+    for k, t in enumerate(ts):
+        arr[k] = _ptr(t)
+    return arr
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fsdp_pack_reduce_scatter(layout: Layout, grads, bucket_bufs, stream=None) -> None:
+    _check(_lib.fsdp_pack_reduce_scatter(layout.handle, _ptr_array(grads), _ptr_array(bucket_bufs),
+                                         _stream(stream)), "fsdp_pack_reduce_scatter")
+
+
+def fsdp_allgather_copy_in(layout: Layout, local_shards, ag_input, stream=None) -> None:
+    _check(_lib.fsdp_allgather_copy_in(layout.handle, _ptr_array(local_shards), _ptr(ag_input),
+                                       _stream(stream)), "fsdp_allgather_copy_in")
+
+
+def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None) -> None:
+    _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), _ptr_array(full_params),
+                                        _stream(stream)), "fsdp_allgather_copy_out")
+
+
+def fsdp_sync_status(layout: Layout, stream=None) -> None:
+    _check(_lib.fsdp_sync_status(layout.handle, _stream(stream)), "fsdp_sync_status")
+
+
+def fsdp_debug_set_wait_fault(fault: int, wait_limit_ns: int) -> None:
+    _lib.fsdp_debug_set_wait_fault(fault, wait_limit_ns)
+
+
+def fsdp_layout_destroy(layout: Layout) -> None:
+    layout.close()

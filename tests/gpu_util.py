@@ -1,0 +1,146 @@
+"""Helpers for the GPU parity tests: guard-banded device buffers at chosen
+byte offsets, and a runner that pushes one fully_shard group through the three
+entry points of the CUDA library and through the oracle on the same inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from fsdp2_gradient_packing_gb300 import workloads as wl
+
+GUARD = 4096
+FILL = 0xA5
+NP = {"f32": np.uint32, "bf16": np.uint16}
+ESZ = {"f32": 4, "bf16": 2}
+
+
+class DevBuf:
+    """``nbytes`` of device memory starting ``offset`` bytes past a 512-byte
+    aligned address, with GUARD canary bytes on both sides.  Everything,
+    including the payload, starts as FILL so unwritten bytes show up."""
+
+    def __init__(self, nbytes: int, offset: int = 0, data: np.ndarray | None = None):
+        self.nbytes = int(nbytes)
+        self.off = GUARD + int(offset)
+        self.raw = torch.full((self.off + self.nbytes + GUARD,), FILL, dtype=torch.uint8, device="cuda")
+        assert self.raw.data_ptr() % 512 == 0
+        if data is not None:
+            self.write(data)
+
+    @property
+    def ptr(self) -> int:
+        return self.raw.data_ptr() + self.off
+
+    def write(self, data: np.ndarray) -> None:
+        b = np.ascontiguousarray(data).view(np.uint8).reshape(-1)
+        assert b.size == self.nbytes
+        if b.size:
+            self.raw[self.off:self.off + b.size].copy_(torch.from_numpy(b.copy()))
+
+    def read(self, dtype=np.uint8) -> np.ndarray:
+        return self.raw[self.off:self.off + self.nbytes].cpu().numpy().view(dtype)
+
+    def guards_ok(self) -> bool:
+        head = self.raw[:self.off]
+        tail = self.raw[self.off + self.nbytes:]
+        return bool((head == FILL).all().item()) and bool((tail == FILL).all().item())
+
+
+def _offset(rng, align: int) -> int:
+    """A byte offset that keeps ``align``-byte alignment but usually breaks 16."""
+    if rng is None:
+        return 0
+    return int(rng.integers(0, 16 // align)) * align
+
+
+class GroupRun:
+    """One group through the CUDA library and the oracle."""
+
+    def __init__(self, fp, specs, W: int, work: wl.Workload, group: int, misalign_seed=None,
+                 specials: float = 0.0):
+        self.fp, self.specs, self.W = fp, list(specs), W
+        self.pl = oracle.plan(oracle.params_from_specs(specs), W)
+        self.L = fp.fsdp_plan_layout(specs, W)
+        self.rng = np.random.default_rng(misalign_seed) if misalign_seed is not None else None
+        self.grads = [wl.grad_values(work, group, i, specials=specials) for i in range(len(specs))]
+        self.shards = []
+        for r in range(W):
+            row = []
+            for i, (s, c) in enumerate(zip(specs, self.pl.chunk)):
+                row.append(wl.shard_values(work, group, i, r, c, max(0, min(c, s.numel - r * c)),
+                                           specials=specials))
+            self.shards.append(row)
+
+    def close(self):
+        self.L.close()
+
+    # -- reduce-scatter copy-in --------------------------------------------
+    def pack(self):
+        fp, pl = self.fp, self.pl
+        g_bufs = [DevBuf(g.nbytes, _offset(self.rng, ESZ[s.grad_dtype]), g) for s, g in zip(self.specs, self.grads)]
+        rho = ["f32" if d == oracle.F32 else "bf16" for d in pl.bucket_dtype]
+        out = [DevBuf(self.W * S * ESZ[r], _offset(self.rng, ESZ[r])) for r, S in zip(rho, pl.bucket_S)]
+        fp.fsdp_pack_reduce_scatter(self.L, [b.ptr for b in g_bufs], [b.ptr for b in out])
+        fp.fsdp_sync_status(self.L)
+        got = [b.read(NP[r]) for b, r in zip(out, rho)]
+        ok = all(b.guards_ok() for b in out + g_bufs)
+        return got, ok
+
+    def pack_expected(self):
+        return oracle.pack_reduce_scatter(self.pl, self.grads)
+
+    # -- all-gather copy-in (every rank into its row) and copy-out ------------
+    def gather(self):
+        fp, pl = self.fp, self.pl
+        gathered = DevBuf(self.W * pl.S_ag, 0)
+        inputs = []
+        for r in range(self.W):
+            bufs = [DevBuf(x.nbytes, _offset(self.rng, ESZ[s.shard_dtype]), x) for s, x in zip(self.specs, self.shards[r])]
+            inputs += bufs
+            fp.fsdp_allgather_copy_in(self.L, [b.ptr for b in bufs], gathered.ptr + r * pl.S_ag)
+        outs = [DevBuf(s.numel * ESZ[s.param_dtype], _offset(self.rng, ESZ[s.param_dtype])) for s in self.specs]
+        fp.fsdp_allgather_copy_out(self.L, gathered.ptr, [b.ptr for b in outs])
+        fp.fsdp_sync_status(self.L)
+        rows = gathered.read()
+        full = [b.read(NP[s.param_dtype]) for b, s in zip(outs, self.specs)]
+        ok = gathered.guards_ok() and all(b.guards_ok() for b in outs + inputs)
+        return rows, full, ok
+
+    def gather_expected(self):
+        rows = np.concatenate([oracle.allgather_copy_in(self.pl, self.shards[r]) for r in range(self.W)]) \
+            if self.W * self.pl.S_ag else np.zeros(0, np.uint8)
+        return rows, oracle.allgather_copy_out(self.pl, rows)
+
+
+def first_mismatch(a: np.ndarray, b: np.ndarray) -> str:
+    if a.shape != b.shape:
+        return f"shape {a.shape} vs {b.shape}"
+    bad = np.flatnonzero(a != b)
+    if bad.size == 0:
+        return "equal"
+    i = int(bad[0])
+    return f"{bad.size} mismatches, first at {i}: got {a[i]:#x} want {b[i]:#x}"
+
+
+def assert_group_parity(fp, specs, W, work, group, misalign_seed=None, specials=0.0):
+    run = GroupRun(fp, specs, W, work, group, misalign_seed, specials)
+    try:
+        got, ok = run.pack()
+        assert ok, "guard bytes around pack buffers changed"
+        for b, (x, y) in enumerate(zip(got, run.pack_expected())):
+            assert np.array_equal(x, y), f"pack bucket {b}: {first_mismatch(x, y)}"
+        rows, full, ok = run.gather()
+        assert ok, "guard bytes around all-gather buffers changed"
+        want_rows, want_full = run.gather_expected()
+        assert np.array_equal(rows, want_rows), f"copy-in: {first_mismatch(rows, want_rows)}"
+        for p, (x, y) in enumerate(zip(full, want_full)):
+            assert np.array_equal(x, y), f"copy-out param {p}: {first_mismatch(x, y)}"
+    finally:
+        run.close()
+
+
+def fp_module():
+    from fsdp2_gradient_packing_gb300 import fsdp_pack
+    return fsdp_pack
+

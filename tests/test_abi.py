@@ -1,0 +1,158 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+that include/*.h declares, plans layouts on the host exactly as the oracle
+does, and rejects bad arguments with the documented status codes."""
+import ctypes
+import glob
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+from fsdp2_gradient_packing_gb300 import _build
+from fsdp2_gradient_packing_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fp():
+    _build.build()
+    from fsdp2_gradient_packing_gb300 import fsdp_pack
+    return fsdp_pack
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \t\*]*?\b(fsdp_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(fp):
+    names = declared_functions()
+    assert "fsdp_pack_reduce_scatter" in names and len(names) >= 10
+    lib = ctypes.CDLL(_build.LIB)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_has_a_function_per_entry_point(fp):
+    for n in declared_functions():
+        assert callable(getattr(fp, n)), n
+
+
+def _compare_with_oracle(fp, specs, W):
+    pl = oracle.plan(oracle.params_from_specs(specs), W)
+    with fp.fsdp_plan_layout_host(specs, W) as L:
+        info = fp.fsdp_layout_query(L)
+        assert info.world_size == W and info.n_params == len(specs)
+        assert info.n_buckets == len(pl.bucket_dtype) and info.n_groups == len(pl.group_pair)
+        assert info.ag_bytes == pl.S_ag and info.has_device_table == 0 and info.device == -1
+        assert info.total_numel == sum(s.numel for s in specs)
+        for p in range(len(specs)):
+            pi = fp.fsdp_layout_param(L, p)
+            assert pi.chunk == pl.chunk[p]
+            assert (pi.bucket, pi.bucket_offset) == (pl.bucket_of[p], pl.bucket_off[p])
+            assert (pi.group, pi.group_offset) == (pl.group_of[p], pl.group_elem_off[p])
+            g = pl.group_of[p]
+            assert pi.ag_byte_offset == pl.group_byte_off[g] + pl.group_elem_off[p] * oracle.DTYPE_SIZE[pl.group_pair[g][1]]
+        for b in range(info.n_buckets):
+            bi = fp.fsdp_layout_bucket(L, b)
+            assert bi.reduce_dtype == pl.bucket_dtype[b] and bi.row_elems == pl.bucket_S[b]
+            assert bi.bytes == W * pl.bucket_S[b] * oracle.DTYPE_SIZE[pl.bucket_dtype[b]]
+            assert bi.n_params == pl.bucket_of.count(b)
+        for g in range(info.n_groups):
+            gi = fp.fsdp_layout_group(L, g)
+            assert (gi.shard_dtype, gi.param_dtype) == pl.group_pair[g]
+            assert gi.byte_offset == pl.group_byte_off[g] and gi.elems == pl.group_elems[g]
+
+
+@pytest.mark.parametrize("make", [
+    lambda: wl.tiny_two_blocks(grouping="linear"), lambda: wl.tiny_two_blocks(grouping="block"),
+    lambda: wl.tiny_two_blocks(grouping="model"), lambda: wl.transformer_500(),
+    lambda: wl.mixed_50m(), lambda: wl.kda_block(W=8, reduce="grad"),
+    lambda: wl.kda_block(W=64, reduce="f32"), lambda: wl.kda_block(W=64, reduce="bf16"),
+])
+def test_host_plan_matches_oracle_on_workloads(fp, make):
+    work = make()
+    for g in work.groups:
+        _compare_with_oracle(fp, g, work.W)
+
+
+def test_host_plan_matches_oracle_on_random_layouts(fp):
+    for seed in range(400):
+        work = wl.random_layout(seed)
+        _compare_with_oracle(fp, work.groups[0], work.W)
+
+
+def test_empty_layout(fp):
+    with fp.fsdp_plan_layout_host([], 4) as L:
+        info = fp.fsdp_layout_query(L)
+        assert (info.n_params, info.n_buckets, info.n_groups, info.ag_bytes) == (0, 0, 0, 0)
+        assert (info.pack_items, info.copy_in_items, info.copy_out_items) == (0, 0, 0)
+
+
+def test_work_items_cover_the_buffers(fp):
+    # One pack item per (rank, parameter) run at most 32 KiB of destination
+    # and 16 KiB of source: the counts follow from the run lengths.
+    work = wl.mixed_50m()
+    with fp.fsdp_plan_layout_host(work.groups[0], 8) as L:
+        info = fp.fsdp_layout_query(L)
+        # 8 ranks x (24 BF16 matrices of 131072 or 524288 elements per rank, cut
+        # at 8192 elements) + 8 ranks x 8 norms of 128 elements
+        runs_bf16 = 8 * 4 * (4 * 131072 + 2 * 524288) // 8192
+        assert info.pack_items == runs_bf16 + 8 * 8
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(W=0), "FSDP_EINVAL"),
+    (dict(numel=-1), "FSDP_EINVAL"),
+    (dict(dtype=7), "FSDP_EINVAL"),
+    (dict(n=4001), "FSDP_EUNSUPPORTED"),
+])
+def test_plan_rejects_bad_arguments(fp, bad, status):
+    W = bad.get("W", 4)
+    n = bad.get("n", 3)
+    descs = [fp.fsdp_param_desc_t(bad.get("numel", 10), bad.get("dtype", 0), 0, 0, 0) for _ in range(n)]
+    with pytest.raises(fp.FsdpError) as e:
+        fp.fsdp_plan_layout_host(descs, W)
+    assert fp.fsdp_status_string(e.value.status) == status
+    assert fp.fsdp_last_error()
+
+
+def test_entry_points_reject_host_only_layout_without_launching(fp):
+    with fp.fsdp_plan_layout_host(wl.tiny_two_blocks().groups[0], 4) as L:
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_pack_reduce_scatter(L, [0x1000], [0x2000], stream=0)
+        assert e.value.status == fp.FSDP_EINVAL
+        with pytest.raises(fp.FsdpError):
+            fp.fsdp_allgather_copy_in(L, [0x1000], 0x2000, stream=0)
+        with pytest.raises(fp.FsdpError):
+            fp.fsdp_allgather_copy_out(L, 0x2000, [0x1000], stream=0)
+
+
+def test_query_index_out_of_range(fp):
+    with fp.fsdp_plan_layout_host(wl.tiny_two_blocks().groups[0], 4) as L:
+        for fn in (fp.fsdp_layout_param, fp.fsdp_layout_bucket, fp.fsdp_layout_group):
+            with pytest.raises(fp.FsdpError):
+                fn(L, 99)
+            with pytest.raises(fp.FsdpError):
+                fn(L, -1)
+
+
+def test_status_strings(fp):
+    names = [fp.fsdp_status_string(s) for s in range(6)]
+    assert names == ["FSDP_OK", "FSDP_EINVAL", "FSDP_ENOMEM", "FSDP_ECUDA", "FSDP_EUNSUPPORTED", "FSDP_ETIMEOUT"]
+    assert fp.fsdp_status_string(99) == "FSDP_UNKNOWN_STATUS"
+
+
+def test_plan_without_gpu_reports_cuda_error(fp):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    with pytest.raises(fp.FsdpError) as e:
+        fp.fsdp_plan_layout(wl.tiny_two_blocks().groups[0], 4)
+    assert e.value.status == fp.FSDP_ECUDA

@@ -1,0 +1,232 @@
+"""GPU parity: every entry point of the CUDA library, called through the C
+ABI, against the CPU oracle on the same seeded inputs.  Every comparison is
+bit-exact (the path only moves and casts bits, so the oracle's result is the
+only correct one).  Output buffers sit between canary bands and start filled
+with a non-zero pattern, so stray writes and skipped padding both show up;
+inputs and outputs are placed at byte offsets that break 16-byte alignment in
+the fuzz cases, to exercise the scalar heads and tails and the shifted reads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fsdp2_gradient_packing_gb300 import workloads as wl
+from gpu_util import DevBuf, ESZ, NP, GroupRun, assert_group_parity, first_mismatch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp():
+    from fsdp2_gradient_packing_gb300 import _build
+    _build.build()
+    from fsdp2_gradient_packing_gb300 import fsdp_pack
+    return fsdp_pack
+
+
+@pytest.mark.parametrize("grouping", ["linear", "block", "model"])
+def test_tiny_two_blocks(fp, grouping):
+    work = wl.tiny_two_blocks(W=4, grouping=grouping)
+    for g, specs in enumerate(work.groups):
+        assert_group_parity(fp, specs, work.W, work, g)
+        assert_group_parity(fp, specs, work.W, work, g, misalign_seed=g + 1, specials=0.2)
+
+
+@pytest.mark.parametrize("chunk", range(6))
+def test_random_layouts_misaligned_with_special_values(fp, chunk):
+    for seed in range(chunk * 60, (chunk + 1) * 60):
+        work = wl.random_layout(seed, max_params=8, max_numel=5000)
+        assert_group_parity(fp, work.groups[0], work.W, work, 0, misalign_seed=seed, specials=0.05)
+
+
+def test_random_long_runs_misaligned(fp):
+    # runs long enough to span several work items and pipeline stages
+    for seed in range(12):
+        work = wl.random_layout(1000 + seed, max_params=5, max_numel=200_000, W_choices=(1, 3, 8, 64))
+        assert_group_parity(fp, work.groups[0], work.W, work, 0, misalign_seed=seed, specials=0.01)
+
+
+def test_transformer500_every_layer(fp):
+    work = wl.transformer_500(W=8)
+    assert work.n_params == 408
+    for g, specs in enumerate(work.groups):
+        assert_group_parity(fp, specs, work.W, work, g)
+
+
+def test_world_size_one_and_sixty_four(fp):
+    for W in (1, 64):
+        work = wl.transformer_500(W=W, layers=2)
+        for g, specs in enumerate(work.groups):
+            assert_group_parity(fp, specs, W, work, g, misalign_seed=W + g, specials=0.01)
+
+
+def test_mixed50m_full_size(fp):
+    """The 50.3M-element group at W=8: all three entry points at full size,
+    compared whole, in the launch configuration the benchmark times."""
+    work = wl.mixed_50m(W=8)
+    assert_group_parity(fp, work.groups[0], 8, work, 0)
+
+
+def _sample_indices(pl, b, rng, n_random):
+    """Random flat indices plus every (rank, parameter) run's first, last and
+    first-padding positions in bucket b."""
+    S = pl.bucket_S[b]
+    idx = [rng.integers(0, pl.W * S, n_random)]
+    edges = []
+    for p, spec in enumerate(pl.params):
+        if pl.bucket_of[p] != b or pl.chunk[p] == 0:
+            continue
+        c, o = pl.chunk[p], pl.bucket_off[p]
+        for r in range(pl.W):
+            valid = max(0, min(c, spec.numel - r * c))
+            for i in (0, 1, c - 2, c - 1, valid - 1, valid, valid + 1):
+                if 0 <= i < c:
+                    edges.append(r * S + o + i)
+    idx.append(np.array(edges, np.int64))
+    return np.unique(np.concatenate(idx))
+
+
+@pytest.mark.parametrize("W,reduce", [(8, "f32"), (64, "f32"), (8, "grad"), (64, "grad"), (8, "bf16")])
+def test_kda_block_full_size(fp, W, reduce):
+    """One block of the 1.75B-parameter KDA-style layout at full size.  The
+    pack output (up to 872 MB) is checked on sampled elements computed one by
+    one by the oracle, including every run's edges; the all-gather copy-in and
+    copy-out are compared whole."""
+    work = wl.kda_block(W=W, reduce=reduce)
+    specs = work.groups[0]
+    run = GroupRun(fp, specs, W, work, 0)
+    try:
+        got, ok = run.pack()
+        assert ok
+        rng = np.random.default_rng(W)
+        for b in range(len(got)):
+            idx = _sample_indices(run.pl, b, rng, 2_000_000)
+            want = oracle.pack_samples(run.pl, run.grads, b, idx)
+            assert np.array_equal(got[b][idx], want), f"bucket {b}: {first_mismatch(got[b][idx], want)}"
+        del got
+        if reduce == "f32":
+            rows, full, ok = run.gather()
+            assert ok
+            want_rows, want_full = run.gather_expected()
+            assert np.array_equal(rows, want_rows), first_mismatch(rows, want_rows)
+            for x, y in zip(full, want_full):
+                assert np.array_equal(x, y), first_mismatch(x, y)
+    finally:
+        run.close()
+
+
+def test_many_parameters_use_the_larger_parameter_blocks(fp):
+    rnd = np.random.default_rng(5)
+    for n in (70, 600, 4000):
+        specs = tuple(wl.ParamSpec(f"p{i}", (int(rnd.integers(0, 40)),), ("f32", "bf16")[i % 2],
+                                   ("f32", "bf16")[(i // 2) % 2], "f32", ("f32", "bf16")[(i // 3) % 2])
+                      for i in range(n))
+        work = wl.Workload(f"many{n}", 4, (specs,), std=1.0, seed=77)
+        assert_group_parity(fp, specs, 4, work, 0, misalign_seed=n)
+
+
+def test_empty_layout_and_empty_parameters(fp):
+    with fp.fsdp_plan_layout([], 8) as L:
+        fp.fsdp_pack_reduce_scatter(L, [], [])
+        fp.fsdp_allgather_copy_in(L, [], None)
+        fp.fsdp_allgather_copy_out(L, None, [])
+        fp.fsdp_sync_status(L)
+    specs = (wl.ParamSpec("z0", (0,), "bf16", "bf16"), wl.ParamSpec("x", (5,)), wl.ParamSpec("z1", (0,)))
+    work = wl.Workload("zeros", 3, (specs,), seed=3)
+    assert_group_parity(fp, specs, 3, work, 0)
+    with fp.fsdp_plan_layout(specs, 3) as L:
+        out = DevBuf(3 * 2 * 4)
+        x = DevBuf(5 * 4, 0, wl.grad_values(work, 0, 1))
+        fp.fsdp_pack_reduce_scatter(L, [None, x.ptr, None], [None, out.ptr])   # NULL for 0-byte tensors
+        fp.fsdp_sync_status(L)
+        assert out.guards_ok()
+
+
+def test_argument_errors_launch_nothing(fp):
+    specs = wl.tiny_two_blocks(grouping="model").groups[0]
+    work = wl.tiny_two_blocks(grouping="model")
+    with fp.fsdp_plan_layout(specs, 4) as L:
+        grads = [DevBuf(s.numel * ESZ[s.grad_dtype], 0, wl.grad_values(work, 0, i)) for i, s in enumerate(specs)]
+        out = DevBuf(4 * 36 * 4)
+        cases = [
+            ([grads[0].ptr + 1] + [g.ptr for g in grads[1:]], [out.ptr]),     # misaligned grad
+            ([g.ptr for g in grads], [out.ptr + 2]),                          # misaligned FP32 bucket
+            ([None] + [g.ptr for g in grads[1:]], [out.ptr]),                 # NULL grad
+            ([g.ptr for g in grads], [None]),                                 # NULL bucket
+        ]
+        for gp, bp in cases:
+            with pytest.raises(fp.FsdpError) as e:
+                fp.fsdp_pack_reduce_scatter(L, gp, bp)
+            assert e.value.status == fp.FSDP_EINVAL
+        with pytest.raises(fp.FsdpError):
+            fp.fsdp_allgather_copy_in(L, [g.ptr for g in grads], out.ptr + 8)   # not 16-byte aligned
+        with pytest.raises(fp.FsdpError):
+            fp.fsdp_allgather_copy_out(L, out.ptr + 8, [g.ptr for g in grads])
+        torch.cuda.synchronize()
+        assert (out.raw == 0xA5).all().item(), "a rejected call wrote to its output"
+
+
+def test_calls_allocate_no_device_memory(fp):
+    work = wl.mixed_50m(W=8)
+    run = GroupRun(fp, work.groups[0], 8, work, 0)
+    try:
+        grads = [torch.from_numpy(g.view(np.int16 if g.dtype == np.uint16 else np.int32)).cuda() for g in run.grads]
+        out = torch.empty(8 * run.pl.bucket_S[0], dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        stats0 = torch.cuda.memory_stats()["allocation.all.allocated"]
+        for _ in range(3):
+            fp.fsdp_pack_reduce_scatter(run.L, grads, [out])
+        torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        assert free1 == free0, "the pack call changed free device memory"
+        assert torch.cuda.memory_stats()["allocation.all.allocated"] == stats0
+        # The FP32 temporary a pre-cast would need: 50,331,648 * 4 B = 192 MiB.
+        assert sum(g.numel() for g in grads if g.dtype == torch.int16) * 4 == 192 * 2**20
+    finally:
+        run.close()
+
+
+def test_nondefault_stream(fp):
+    work = wl.transformer_500(W=8, layers=1)
+    specs = work.groups[0]
+    run = GroupRun(fp, specs, 8, work, 0)
+    try:
+        grads = [DevBuf(g.nbytes, 0, g) for g in run.grads]
+        out = DevBuf(8 * run.pl.bucket_S[0] * 4)
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [out.ptr])   # current stream = s
+        s.synchronize()
+        want = run.pack_expected()[0]
+        assert np.array_equal(out.read(np.uint32), want)
+    finally:
+        run.close()
+
+
+def test_bounded_wait_reports_timeout_and_recovers(fp):
+    """A pipeline stage that is never armed makes its consumers hit the wait
+    limit: the kernel returns, fsdp_sync_status reports FSDP_ETIMEOUT, and
+    the next call runs normally.  No fault, no hang."""
+    work = wl.transformer_500(W=8, layers=1)
+    specs = work.groups[0]
+    run = GroupRun(fp, specs, 8, work, 0)
+    try:
+        grads = [DevBuf(g.nbytes, 0, g) for g in run.grads]
+        out = DevBuf(8 * run.pl.bucket_S[0] * 4)
+        fp.fsdp_debug_set_wait_fault(1, 50_000_000)   # 50 ms
+        try:
+            fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [out.ptr])
+            with pytest.raises(fp.FsdpError) as e:
+                fp.fsdp_sync_status(run.L)
+            assert e.value.status == fp.FSDP_ETIMEOUT
+        finally:
+            fp.fsdp_debug_set_wait_fault(0, 0)
+        fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [out.ptr])
+        fp.fsdp_sync_status(run.L)
+        assert np.array_equal(out.read(np.uint32), run.pack_expected()[0])
+        assert out.guards_ok()
+    finally:
+        run.close()
