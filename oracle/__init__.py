@@ -283,3 +283,46 @@ def params_from_specs(specs):
     """Oracle parameter descriptors from workload specs (dtype strings)."""
     return [Param(s.numel, _CODE[s.grad_dtype], _CODE[s.reduce_dtype],
                   _CODE[s.shard_dtype], _CODE[s.param_dtype]) for s in specs]
+
+
+# ---------------------------------------------------------------------------
+# One run at a time (the same loops, entered per segment): lets the CPU
+# baseline time bounded samples of a workload.
+# ---------------------------------------------------------------------------
+def _bind_segments(lib):
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.oracle_pack_segment.argtypes = [I32, I64, I32, I64, I64, I32, I64, P, P]
+    lib.oracle_allgather_copy_in_segment.argtypes = [I64, I32, I32, I64, I64, P, P]
+    lib.oracle_allgather_copy_out_segment.argtypes = [I32, I64, I64, I32, I64, I64, I64, P, P]
+    for n in ("oracle_pack_segment", "oracle_allgather_copy_in_segment", "oracle_allgather_copy_out_segment"):
+        getattr(lib, n).restype = None
+    return lib
+
+
+def pack_segment(pl: Plan, grads, bufs, r: int, p: int) -> None:
+    """Row r's slots of parameter p in its bucket buffer (bufs as from pack_reduce_scatter)."""
+    lib = _bind_segments(_load())
+    b = pl.bucket_of[p]
+    lib.oracle_pack_segment(r, pl.params[p].numel, pl.params[p].grad_dtype, pl.chunk[p], pl.bucket_off[p],
+                            pl.bucket_dtype[b], pl.bucket_S[b], grads[p].ctypes.data, bufs[b].ctypes.data)
+
+
+def allgather_copy_in_clear(pl: Plan, ag_in: np.ndarray) -> None:
+    """The zero bytes of one rank's all-gather input (gaps and tail included)."""
+    ag_in[:] = 0
+
+
+def allgather_copy_in_segment(pl: Plan, shards, ag_in: np.ndarray, p: int) -> None:
+    lib = _bind_segments(_load())
+    g = pl.group_of[p]
+    lib.oracle_allgather_copy_in_segment(pl.chunk[p], pl.params[p].shard_dtype, pl.params[p].param_dtype,
+                                         pl.group_elem_off[p], pl.group_byte_off[g], shards[p].ctypes.data,
+                                         ag_in.ctypes.data)
+
+
+def allgather_copy_out_segment(pl: Plan, ag_out: np.ndarray, params, p: int, r: int) -> None:
+    lib = _bind_segments(_load())
+    g = pl.group_of[p]
+    lib.oracle_allgather_copy_out_segment(r, pl.params[p].numel, pl.chunk[p], pl.params[p].param_dtype,
+                                          pl.group_elem_off[p], pl.group_byte_off[g], pl.S_ag,
+                                          ag_out.ctypes.data, params[p].ctypes.data)

@@ -165,27 +165,32 @@ static void store_zero(void *dst, int32_t ddt, int64_t di) {
  *   buf_b[r*S_b + o_p + i] = cast_{g_p -> rho_b}(grad_p[j])  if j < n_p
  *                          = +0                              otherwise
  * ------------------------------------------------------------------------ */
+/* One (bucket, rank, parameter) run of the loops below: the c_p slots that
+ * parameter p contributes to row r of its bucket buffer. */
+void oracle_pack_segment(int32_t r, int64_t numel, int32_t grad_dtype, int64_t chunk,
+                         int64_t bucket_off, int32_t rho, int64_t S_b, const void *grad, void *buf) {
+  for (int64_t i = 0; i < chunk; ++i) {
+    int64_t j = (int64_t)r * chunk + i;
+    int64_t d = (int64_t)r * S_b + bucket_off + i;
+    if (j < numel)
+      cast_element(grad, grad_dtype, j, buf, rho, d);
+    else
+      store_zero(buf, rho, d);
+  }
+}
+
 void oracle_pack_reduce_scatter(int32_t W, int32_t n_params, const int64_t *numel,
                                 const int32_t *grad_dtype, const int64_t *chunk,
                                 const int32_t *bucket_of, const int64_t *bucket_off,
                                 int32_t n_buckets, const int32_t *bucket_dtype,
                                 const int64_t *bucket_S, const void *const *grads,
                                 void *const *bufs) {
-  for (int32_t b = 0; b < n_buckets; ++b) {
-    for (int32_t r = 0; r < W; ++r) {
-      for (int32_t p = 0; p < n_params; ++p) {
-        if (bucket_of[p] != b) continue;
-        for (int64_t i = 0; i < chunk[p]; ++i) {
-          int64_t j = (int64_t)r * chunk[p] + i;
-          int64_t d = (int64_t)r * bucket_S[b] + bucket_off[p] + i;
-          if (j < numel[p])
-            cast_element(grads[p], grad_dtype[p], j, bufs[b], bucket_dtype[b], d);
-          else
-            store_zero(bufs[b], bucket_dtype[b], d);
-        }
-      }
-    }
-  }
+  for (int32_t b = 0; b < n_buckets; ++b)
+    for (int32_t r = 0; r < W; ++r)
+      for (int32_t p = 0; p < n_params; ++p)
+        if (bucket_of[p] == b)
+          oracle_pack_segment(r, numel[p], grad_dtype[p], chunk[p], bucket_off[p], bucket_dtype[b],
+                              bucket_S[b], grads[p], bufs[b]);
 }
 
 /* Value of one element of bucket b at flat index idx (in [0, W*S_b)), computed
@@ -227,21 +232,26 @@ void oracle_pack_samples(int32_t n_params, const int64_t *numel, const int32_t *
  * then for every group g, parameter p of g, and i < c_p:
  *   ag_in[G_g + (e_p + i)*size(pi_p)] = cast_{sigma_p -> pi_p}(shard_p[i])
  * ------------------------------------------------------------------------ */
+/* Parameter p's part of the loops below: its c_p cast elements. */
+void oracle_allgather_copy_in_segment(int64_t chunk, int32_t shard_dtype, int32_t param_dtype,
+                                      int64_t group_elem_off, int64_t group_byte_off,
+                                      const void *shard, uint8_t *ag_in) {
+  void *base = ag_in + group_byte_off;
+  for (int64_t i = 0; i < chunk; ++i)
+    cast_element(shard, shard_dtype, i, base, param_dtype, group_elem_off + i);
+}
+
 void oracle_allgather_copy_in(int32_t n_params, const int64_t *chunk,
                               const int32_t *shard_dtype, const int32_t *param_dtype,
                               const int32_t *group_of, const int64_t *group_elem_off,
                               int32_t n_groups, const int64_t *group_byte_off, int64_t S_ag,
                               const void *const *shards, uint8_t *ag_in) {
   memset(ag_in, 0, (size_t)S_ag);
-  for (int32_t g = 0; g < n_groups; ++g) {
-    for (int32_t p = 0; p < n_params; ++p) {
-      if (group_of[p] != g) continue;
-      void *base = ag_in + group_byte_off[g];
-      for (int64_t i = 0; i < chunk[p]; ++i)
-        cast_element(shards[p], shard_dtype[p], i, base, param_dtype[p],
-                     group_elem_off[p] + i);
-    }
-  }
+  for (int32_t g = 0; g < n_groups; ++g)
+    for (int32_t p = 0; p < n_params; ++p)
+      if (group_of[p] == g)
+        oracle_allgather_copy_in_segment(chunk[p], shard_dtype[p], param_dtype[p], group_elem_off[p],
+                                         group_byte_off[g], shards[p], ag_in);
 }
 
 /* ---------------------------------------------------------------------------
@@ -252,21 +262,26 @@ void oracle_allgather_copy_in(int32_t n_params, const int64_t *chunk,
  *               i.e. the bytes at r*S_ag + G_g + (e_p + i)*size(pi_p).
  * No cast: the gathered dtype is param_dtype.  Padding is dropped.
  * ------------------------------------------------------------------------ */
+/* One (parameter, rank) run of the loops below. */
+void oracle_allgather_copy_out_segment(int32_t r, int64_t numel, int64_t chunk, int32_t param_dtype,
+                                       int64_t group_elem_off, int64_t group_byte_off, int64_t S_ag,
+                                       const uint8_t *ag_out, void *param) {
+  int64_t sz = dtype_size(param_dtype);
+  for (int64_t i = 0; i < chunk; ++i) {
+    int64_t j = (int64_t)r * chunk + i;
+    if (j >= numel) continue;
+    const uint8_t *from = ag_out + (int64_t)r * S_ag + group_byte_off + (group_elem_off + i) * sz;
+    memcpy((uint8_t *)param + j * sz, from, (size_t)sz);
+  }
+}
+
 void oracle_allgather_copy_out(int32_t W, int32_t n_params, const int64_t *numel,
                                const int64_t *chunk, const int32_t *param_dtype,
                                const int32_t *group_of, const int64_t *group_elem_off,
                                const int64_t *group_byte_off, int64_t S_ag,
                                const uint8_t *ag_out, void *const *params) {
-  for (int32_t p = 0; p < n_params; ++p) {
-    int64_t sz = dtype_size(param_dtype[p]);
-    for (int32_t r = 0; r < W; ++r) {
-      for (int64_t i = 0; i < chunk[p]; ++i) {
-        int64_t j = (int64_t)r * chunk[p] + i;
-        if (j >= numel[p]) continue;
-        const uint8_t *from = ag_out + (int64_t)r * S_ag + group_byte_off[group_of[p]] +
-                              (group_elem_off[p] + i) * sz;
-        memcpy((uint8_t *)params[p] + j * sz, from, (size_t)sz);
-      }
-    }
-  }
+  for (int32_t p = 0; p < n_params; ++p)
+    for (int32_t r = 0; r < W; ++r)
+      oracle_allgather_copy_out_segment(r, numel[p], chunk[p], param_dtype[p], group_elem_off[p],
+                                        group_byte_off[group_of[p]], S_ag, ag_out, params[p]);
 }

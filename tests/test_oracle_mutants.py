@@ -17,20 +17,20 @@ import test_oracle_pins as pins
 
 MUTANTS = {
     "pack: source index off by one":
-        ("int64_t j = (int64_t)r * chunk[p] + i;\n          int64_t d",
-         "int64_t j = (int64_t)r * chunk[p] + i + (i > 0);\n          int64_t d"),
+        ("int64_t j = (int64_t)r * chunk + i;\n    int64_t d",
+         "int64_t j = (int64_t)r * chunk + i + (i > 0);\n    int64_t d"),
     "pack: last real element treated as padding":
-        ("if (j < numel[p])\n            cast_element(grads[p]",
-         "if (j + 1 < numel[p])\n            cast_element(grads[p]"),
+        ("if (j < numel)\n      cast_element(grad, grad_dtype, j, buf, rho, d);",
+         "if (j + 1 < numel)\n      cast_element(grad, grad_dtype, j, buf, rho, d);"),
     "pack: padding filled with wrapped values":
-        ("else\n            store_zero(bufs[b], bucket_dtype[b], d);",
-         "else\n            cast_element(grads[p], grad_dtype[p], j % numel[p], bufs[b], bucket_dtype[b], d);"),
+        ("else\n      store_zero(buf, rho, d);\n  }\n}\n\nvoid oracle_pack_reduce_scatter",
+         "else\n      cast_element(grad, grad_dtype, j % numel, buf, rho, d);\n  }\n}\n\nvoid oracle_pack_reduce_scatter"),
     "pack: bucket offset dropped":
-        ("(int64_t)r * bucket_S[b] + bucket_off[p] + i;",
-         "(int64_t)r * bucket_S[b] + i;"),
+        ("(int64_t)r * S_b + bucket_off + i;",
+         "(int64_t)r * S_b + i;"),
     "pack: rank stride uses chunk instead of row length":
-        ("(int64_t)r * bucket_S[b] + bucket_off[p] + i;",
-         "(int64_t)r * chunk[p] + bucket_off[p] + i;"),
+        ("(int64_t)r * S_b + bucket_off + i;",
+         "(int64_t)r * chunk + bucket_off + i;"),
     "rne: ties always round down":
         ("if (d_lo < d_hi) return toward_zero;", "if (d_lo <= d_hi) return toward_zero;"),
     "rne: ties to odd":
@@ -42,15 +42,16 @@ MUTANTS = {
     "bf16 decode: exponent bias wrong":
         ("mag = ldexp(128.0 + (double)f, e - 127 - 7);", "mag = ldexp(128.0 + (double)f, e - 126 - 7);"),
     "copy-in: element offset in group dropped":
-        ("cast_element(shards[p], shard_dtype[p], i, base, param_dtype[p],\n                     group_elem_off[p] + i);",
-         "cast_element(shards[p], shard_dtype[p], i, base, param_dtype[p],\n                     i);"),
+        ("cast_element(shard, shard_dtype, i, base, param_dtype, group_elem_off + i);",
+         "cast_element(shard, shard_dtype, i, base, param_dtype, i);"),
     "copy-in: gap bytes not cleared":
         ("memset(ag_in, 0, (size_t)S_ag);", "memset(ag_in, 0xAB, (size_t)S_ag);"),
     "copy-out: group start dropped":
-        ("(int64_t)r * S_ag + group_byte_off[group_of[p]] +", "(int64_t)r * S_ag +"),
-    "copy-out: rank rows transposed":
-        ("int64_t j = (int64_t)r * chunk[p] + i;\n        if (j >= numel[p]) continue;",
-         "int64_t j = (int64_t)(W - 1 - r) * chunk[p] + i;\n        if (j >= numel[p]) continue;"),
+        ("(int64_t)r * S_ag + group_byte_off + (group_elem_off + i) * sz;",
+         "(int64_t)r * S_ag + (group_elem_off + i) * sz;"),
+    "copy-out: row stride taken as the chunk":
+        ("const uint8_t *from = ag_out + (int64_t)r * S_ag + group_byte_off",
+         "const uint8_t *from = ag_out + (int64_t)r * chunk * sz + group_byte_off"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and callable(getattr(pins, n))]

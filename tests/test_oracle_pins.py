@@ -450,3 +450,29 @@ def test_bf16_to_f32_exact_for_every_pattern():
     nan = ((h & 0x7F80) == 0x7F80) & ((h & 0x7F) != 0)
     assert np.array_equal(got[~nan], torch_cast(h[~nan], BF16, F32))
     assert np.array_equal(got[nan], h[nan].astype(np.uint32) << np.uint32(16))
+
+
+def test_segment_entry_points_compose_to_the_whole_operations():
+    rng = np.random.default_rng(43)
+    params = [Param(37, BF16, F32, F32, BF16), Param(5, F32, BF16, BF16, BF16), Param(64, F32, F32, F32, F32)]
+    W = 4
+    pl = plan(params, W)
+    grads = [rand_bits(rng, p.numel, p.grad_dtype) for p in params]
+    whole = oracle.pack_reduce_scatter(pl, grads)
+    parts = [np.full_like(b, 0xAB) for b in whole]
+    for r in range(W):
+        for p in range(len(params)):
+            oracle.pack_segment(pl, grads, parts, r, p)
+    assert all(np.array_equal(a, b) for a, b in zip(parts, whole))
+    shards = [rand_bits(rng, c, p.shard_dtype) for p, c in zip(params, pl.chunk)]
+    row = np.full(pl.S_ag, 0xAB, np.uint8)
+    oracle.allgather_copy_in_clear(pl, row)
+    for p in range(len(params)):
+        oracle.allgather_copy_in_segment(pl, shards, row, p)
+    assert np.array_equal(row, oracle.allgather_copy_in(pl, shards))
+    gathered = np.concatenate([row] * W)
+    full = [np.zeros(p.numel, oracle.DTYPE_NP[p.param_dtype]) for p in params]
+    for p in range(len(params)):
+        for r in range(W):
+            oracle.allgather_copy_out_segment(pl, gathered, full, p, r)
+    assert all(np.array_equal(a, b) for a, b in zip(full, oracle.allgather_copy_out(pl, gathered)))
