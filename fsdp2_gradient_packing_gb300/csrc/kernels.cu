@@ -48,9 +48,10 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kStages = 4;
-// Each stage holds kStageBytes plus 16 bytes of slack: the funnel read of the
-// last vector may touch one word past the staged bytes.
-constexpr int kStageStride = (int)kStageBytes + 16;
+// Each stage holds a 64-byte header (the item, see StageHeader) and
+// kStageBytes of data plus 16 bytes of slack: the funnel read of the last
+// vector may touch one word past the staged bytes.
+constexpr int kStageStride = 64 + (int)kStageBytes + 16;
 constexpr int kSmemBytes = kStages * kStageStride + 2 * kStages * 8;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -129,15 +130,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
   }
 }
 
+// Programmatic dependent launch.  Every launch allows the next kernel on the
+// stream to be scheduled early (launch_dependents), and waits for the
+// previous kernel on the stream to finish and publish its memory
+// (griddepcontrol.wait) before touching any input or output.  Only the
+// immutable work table is read before the wait.
+__device__ __forceinline__ void wait_for_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // One TMA bulk copy global -> shared, completion counted on `bar` in bytes.
-// Both addresses are 16-byte aligned and `bytes` is a multiple of 16.
+// Both addresses are 16-byte aligned and `bytes` is a multiple of 16.  The
+// source is read exactly once, so its lines are marked first to be evicted
+// from L2, which leaves L2 to the destination's write-combining.
 __device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
                                               uint64_t *bar) {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
           smem_addr(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// One aligned 16-byte store of the destination.
+__device__ __forceinline__ void store_vec(uint4 *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+  *d = make_uint4(a0, a1, a2, a3);
 }
 
 // ---------------------------------------------------------------------------
@@ -211,18 +229,36 @@ __device__ __forceinline__ Interior interior_of(const char *src, int src_bytes) 
   return in;
 }
 
-// Consumer side of one item.  `stage` holds the item's interior.  `ct` is the
-// consumer thread index in [0, kConsumers).
+// What the producer tells the consumers about the item in a stage: written to
+// shared memory before the stage's "full" barrier is armed, so consumers read
+// it from shared memory after their wait instead of going back to global
+// memory for the work item.
+struct StageHeader {
+  const char *src;  // first source element of the item
+  char *dst;        // first destination element
+  int32_t n_copy;
+  int32_t n_total;
+  int32_t kind;     // kSkipItem: nothing to do (refused by the producer)
+  int32_t reserved;
+};
+constexpr int kHeaderBytes = 64;
+static_assert(sizeof(StageHeader) <= kHeaderBytes, "stage header too large");
+constexpr int32_t kSkipItem = -1;
+
+// Consumer side of one item.  `stage` holds the item's staged interior.
+// `ct` is the consumer thread index in [0, kConsumers).  Each thread handles
+// kBatch destination vectors per round: it reads all their source words from
+// shared memory first, then converts and stores them.
+constexpr int kBatch = 1;
+
 template <int KIND>
-__device__ __forceinline__ void consume_item(const WorkItem &w, const void *src_base, void *dst_base,
+__device__ __forceinline__ void consume_item(const char *src, char *dst, int n_copy, int n_total,
                                              const uint8_t *stage, int ct) {
   using S = typename Traits<KIND>::S;
   using D = typename Traits<KIND>::D;
   constexpr int DU = 16 / (int)sizeof(D);      // elements per destination vector
   constexpr int SW = DU * (int)sizeof(S) / 4;  // source words per vector (2, 4 or 8)
-  const char *src = reinterpret_cast<const char *>(src_base) + w.src_off * (int64_t)sizeof(S);
-  char *dst = reinterpret_cast<char *>(dst_base) + w.dst_off * (int64_t)sizeof(D);
-  const int n_total = w.n_total, n_copy = w.n_copy;
+  constexpr int SB = DU * (int)sizeof(S);      // source bytes per vector
   const Interior in = interior_of(src, n_copy * (int)sizeof(S));
 
   // Destination: scalar head to the first 16-byte boundary, vectors, tail.
@@ -233,47 +269,61 @@ __device__ __forceinline__ void consume_item(const WorkItem &w, const void *src_
   if (ct < h) scalar_elem<KIND>(src, dst, ct, n_copy);
   if (tail0 + ct < n_total) scalar_elem<KIND>(src, dst, tail0 + ct, n_copy);
 
+  // Every vector's source starts at the same byte phase inside the stage.
+  const int rb = ((h * (int)sizeof(S) - in.lo) & 3) * 8;
   const uint32_t *stage32 = reinterpret_cast<const uint32_t *>(stage);
-  for (int j = ct; j < nvec; j += kConsumers) {
-    const int e0 = h + j * DU;
-    uint4 *d = reinterpret_cast<uint4 *>(dst + e0 * (int)sizeof(D));
-    if (e0 >= n_copy) {
-      *d = make_uint4(0u, 0u, 0u, 0u);
-      continue;
-    }
-    const int s_lo = e0 * (int)sizeof(S);
-    if (e0 + DU <= n_copy && s_lo >= in.lo && s_lo + DU * (int)sizeof(S) <= in.hi) {
-      const int off = s_lo - in.lo;  // byte offset inside the stage (even)
-      const int wi = off >> 2;
-      const int rb = (off & 3) * 8;
-      uint32_t wv[SW + 1], s[SW];
+  for (int base = ct; base < nvec; base += kBatch * kConsumers) {
+    uint32_t wv[kBatch][SW + 1];
+    int mode[kBatch];  // 0 none, 1 staged vector, 2 all padding, 3 element by element
 #pragma unroll
-      for (int k = 0; k <= SW; ++k) wv[k] = stage32[wi + k];
+    for (int b = 0; b < kBatch; ++b) {
+      const int j = base + b * kConsumers;
+      const int e0 = h + j * DU;
+      const int s_lo = e0 * (int)sizeof(S);
+      mode[b] = j >= nvec ? 0
+                : e0 >= n_copy ? 2
+                : (e0 + DU <= n_copy && s_lo >= in.lo && s_lo + SB <= in.hi) ? 1
+                                                                               : 3;
+      if (mode[b] == 1) {
+        const int wi = (s_lo - in.lo) >> 2;
 #pragma unroll
-      for (int k = 0; k < SW; ++k) s[k] = __funnelshift_r(wv[k], wv[k + 1], rb);
-      uint32_t o[4];
-      if constexpr (KIND == KIND_BF16_F32) {
-        o[0] = s[0] << 16;
-        o[1] = s[0] & 0xFFFF0000u;
-        o[2] = s[1] << 16;
-        o[3] = s[1] & 0xFFFF0000u;
-      } else if constexpr (KIND == KIND_F32_BF16) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16_bits(s[2 * i]) | (f32_to_bf16_bits(s[2 * i + 1]) << 16);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = s[i];
+        for (int k = 0; k <= SW; ++k) wv[b][k] = stage32[wi + k];
       }
-      *d = make_uint4(o[0], o[1], o[2], o[3]);
-    } else {
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int e0 = h + (base + b * kConsumers) * DU;
+      uint4 *d = reinterpret_cast<uint4 *>(dst + e0 * (int)sizeof(D));
+      if (mode[b] == 1) {
+        uint32_t sw[SW];
+#pragma unroll
+        for (int k = 0; k < SW; ++k) sw[k] = __funnelshift_r(wv[b][k], wv[b][k + 1], rb);
+        uint32_t o[4];
+        if constexpr (KIND == KIND_BF16_F32) {
+          o[0] = sw[0] << 16;
+          o[1] = sw[0] & 0xFFFF0000u;
+          o[2] = sw[1] << 16;
+          o[3] = sw[1] & 0xFFFF0000u;
+        } else if constexpr (KIND == KIND_F32_BF16) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16_bits(sw[2 * i]) | (f32_to_bf16_bits(sw[2 * i + 1]) << 16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = sw[i];
+        }
+        store_vec(d, o[0], o[1], o[2], o[3]);
+      } else if (mode[b] == 2) {
+        store_vec(d, 0u, 0u, 0u, 0u);
+      } else if (mode[b] == 3) {
 #pragma unroll 1
-      for (int e = 0; e < DU; ++e) scalar_elem<KIND>(src, dst, e0 + e, n_copy);
+        for (int e = 0; e < DU; ++e) scalar_elem<KIND>(src, dst, e0 + e, n_copy);
+      }
     }
   }
 }
 
 template <int NSLOT>
-__global__ void __launch_bounds__(kThreads) walk_kernel(const __grid_constant__ LaunchArgs<NSLOT> a) {
+__global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant__ LaunchArgs<NSLOT> a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageStride);
   uint64_t *empty = full + kStages;
@@ -284,15 +334,23 @@ __global__ void __launch_bounds__(kThreads) walk_kernel(const __grid_constant__ 
     }
     fence_mbar_init();
   }
+  allow_next_grid();
   __syncthreads();
 
   const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
   if (warp == 0) {
     if (lane != 0) return;
-    // Producer.
+    // Producer.  The next item's descriptor is fetched one item ahead; the
+    // first one before waiting for the previous kernel on the stream.
     int64_t k = 0;
     bool skipped_first = false;
-    for (int64_t i = blockIdx.x; i < a.n_items; i += gridDim.x, ++k) {
+    int64_t i = blockIdx.x;
+    WorkItem next{};
+    if (i < a.n_items) next = a.items[i];
+    wait_for_previous_grid();
+    for (; i < a.n_items; i += gridDim.x, ++k) {
+      const WorkItem w = next;
+      if (i + gridDim.x < a.n_items) next = a.items[i + gridDim.x];
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
@@ -303,17 +361,23 @@ __global__ void __launch_bounds__(kThreads) walk_kernel(const __grid_constant__ 
         skipped_first = true;
         continue;
       }
-      const WorkItem w = a.items[i];
-      const int sz = (w.kind & 1) ? 2 : 4;
-      const char *src = reinterpret_cast<const char *>(a.slot[w.src_slot]) + w.src_off * (int64_t)sz;
-      const Interior in = interior_of(src, w.n_copy * sz);
+      const int ss = (w.kind & 1) ? 2 : 4, ds = (w.kind & 2) ? 2 : 4;
+      const char *src = reinterpret_cast<const char *>(a.slot[w.src_slot]) + w.src_off * (int64_t)ss;
+      const Interior in = interior_of(src, w.n_copy * ss);
       uint32_t bytes = (uint32_t)(in.hi - in.lo);
-      if (bytes > (uint32_t)kStageBytes) {  // never planned; consumers skip such an item
+      StageHeader *hd = reinterpret_cast<StageHeader *>(smem + s * kStageStride);
+      hd->src = src;
+      hd->dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[w.dst_slot])) + w.dst_off * (int64_t)ds;
+      hd->n_copy = w.n_copy;
+      hd->n_total = w.n_total;
+      hd->kind = w.kind;
+      if (bytes > (uint32_t)kStageBytes) {  // never planned; the consumers skip it
         atomicOr(a.status, kStatusBadItem);
+        hd->kind = kSkipItem;
         bytes = 0;
       }
       mbar_arrive_expect_tx(&full[s], bytes);
-      if (bytes) bulk_copy_g2s(smem + s * kStageStride, src + in.lo, bytes, &full[s]);
+      if (bytes) bulk_copy_g2s(smem + s * kStageStride + kHeaderBytes, src + in.lo, bytes, &full[s]);
     }
     // Leave no bulk copy in flight when this thread exits: wait for the last
     // armed phase of every stage (consumers may have left early).
@@ -326,6 +390,7 @@ __global__ void __launch_bounds__(kThreads) walk_kernel(const __grid_constant__ 
   }
 
   // Consumers.
+  wait_for_previous_grid();
   const int ct = (int)threadIdx.x - 32;
   int64_t k = 0;
   for (int64_t i = blockIdx.x; i < a.n_items; i += gridDim.x, ++k) {
@@ -334,25 +399,14 @@ __global__ void __launch_bounds__(kThreads) walk_kernel(const __grid_constant__ 
       if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
       return;
     }
-    const WorkItem w = a.items[i];
-    const void *sp = a.slot[w.src_slot];
-    {
-      // The producer refuses an item whose interior exceeds a stage; skip it too.
-      const int sz = (w.kind & 1) ? 2 : 4;
-      const Interior in = interior_of(reinterpret_cast<const char *>(sp) + w.src_off * (int64_t)sz, w.n_copy * sz);
-      if (in.hi - in.lo > (int)kStageBytes) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        continue;
-      }
-    }
-    void *dp = const_cast<void *>(a.slot[w.dst_slot]);
-    const uint8_t *stage = smem + s * kStageStride;
-    switch (w.kind) {
-      case KIND_F32_F32: consume_item<KIND_F32_F32>(w, sp, dp, stage, ct); break;
-      case KIND_BF16_F32: consume_item<KIND_BF16_F32>(w, sp, dp, stage, ct); break;
-      case KIND_F32_BF16: consume_item<KIND_F32_BF16>(w, sp, dp, stage, ct); break;
-      default: consume_item<KIND_BF16_BF16>(w, sp, dp, stage, ct); break;
+    const StageHeader hd = *reinterpret_cast<const StageHeader *>(smem + s * kStageStride);
+    const uint8_t *stage = smem + s * kStageStride + kHeaderBytes;
+    switch (hd.kind) {
+      case KIND_F32_F32: consume_item<KIND_F32_F32>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
+      case KIND_BF16_F32: consume_item<KIND_BF16_F32>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
+      case KIND_F32_BF16: consume_item<KIND_F32_BF16>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
+      case KIND_BF16_BF16: consume_item<KIND_BF16_BF16>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
+      default: break;  // refused item
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -381,9 +435,21 @@ fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptr
   a.reserved = 0;
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
+  // Programmatic stream serialization: this launch may be scheduled while the
+  // previous kernel on the stream drains; the kernel waits for it before
+  // touching memory (see wait_for_previous_grid).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)L->op[op].grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void *args[] = {&a};
-  cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void *>(&walk_kernel<NSLOT>),
-                                   dim3((unsigned)L->op[op].grid), dim3(kThreads), args, kSmemBytes, stream);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<NSLOT>), args);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
   clear_error();
   return FSDP_OK;

@@ -198,7 +198,11 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
-def _ptr_array(ts):
+def pointer_array(ts):
+    """A C array of device pointers (tensors, ints or None); pass it in place
+    of a list to skip re-marshalling on every call."""
+    if isinstance(ts, ctypes.Array):
+        return ts
     arr = (_P * max(1, len(ts)))()
     for k, t in enumerate(ts):
         arr[k] = _ptr(t)
@@ -215,17 +219,17 @@ def _stream(stream) -> int | None:
 
 
 def fsdp_pack_reduce_scatter(layout: Layout, grads, bucket_bufs, stream=None) -> None:
-    _check(_lib.fsdp_pack_reduce_scatter(layout.handle, _ptr_array(grads), _ptr_array(bucket_bufs),
+    _check(_lib.fsdp_pack_reduce_scatter(layout.handle, pointer_array(grads), pointer_array(bucket_bufs),
                                          _stream(stream)), "fsdp_pack_reduce_scatter")
 
 
 def fsdp_allgather_copy_in(layout: Layout, local_shards, ag_input, stream=None) -> None:
-    _check(_lib.fsdp_allgather_copy_in(layout.handle, _ptr_array(local_shards), _ptr(ag_input),
+    _check(_lib.fsdp_allgather_copy_in(layout.handle, pointer_array(local_shards), _ptr(ag_input),
                                        _stream(stream)), "fsdp_allgather_copy_in")
 
 
 def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None) -> None:
-    _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), _ptr_array(full_params),
+    _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), pointer_array(full_params),
                                         _stream(stream)), "fsdp_allgather_copy_out")
 
 

@@ -96,14 +96,14 @@ def test_empty_layout(fp):
 
 
 def test_work_items_cover_the_buffers(fp):
-    # One pack item per (rank, parameter) run at most 32 KiB of destination
-    # and 16 KiB of source: the counts follow from the run lengths.
+    # Pack items are (rank, parameter) runs cut to at most 16 KiB of
+    # destination and 8 KiB of source: the counts follow from the run lengths.
     work = wl.mixed_50m()
     with fp.fsdp_plan_layout_host(work.groups[0], 8) as L:
         info = fp.fsdp_layout_query(L)
         # 8 ranks x (24 BF16 matrices of 131072 or 524288 elements per rank, cut
-        # at 8192 elements) + 8 ranks x 8 norms of 128 elements
-        runs_bf16 = 8 * 4 * (4 * 131072 + 2 * 524288) // 8192
+        # at 4096 elements) + 8 ranks x 8 norms of 128 elements
+        runs_bf16 = 8 * 4 * (4 * 131072 + 2 * 524288) // 4096
         assert info.pack_items == runs_bf16 + 8 * 8
 
 
