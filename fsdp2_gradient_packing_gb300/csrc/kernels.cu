@@ -37,6 +37,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "layout.h"
@@ -495,6 +496,80 @@ cudaError_t allow_smem() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free pack (fsdp_pack_reduce_scatter_noalloc).
+//
+// Some callers cannot allocate device memory at the point where they pack:
+// code that runs while another component owns every byte of the device's
+// memory budget, code inside an allocator or memory-pool callback (where a
+// cudaMalloc would re-enter the allocator), and runtimes that forbid device
+// allocation after start-up.  For them the pack can run with its scratch --
+// the status word and the work table that the kernel walks -- in this
+// file-scope array instead of memory from fsdp_plan_layout.  The array is part
+// of the loaded module: every GPU that loads the library holds it until the
+// process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kNoAllocTableOffset = 256;               // status word, padded
+constexpr int64_t kNoAllocMaxItems = (int64_t)((kNoAllocScratchBytes - kNoAllocTableOffset) / sizeof(WorkItem));
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Per-device set-up, done once by the first call on that device: the device
+// address of the array (in host code its name is only a host-side stand-in)
+// and the resident grid size.
+struct NoAllocDevice {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  unsigned char *scratch = nullptr;
+  int64_t resident = 0;
+};
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+
+void noalloc_setup(NoAllocDevice &nd, int dev) {
+  int sms = 0, per_sm = 0;
+  void *ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<kSlotsSmall>, kThreads, kSmemBytes);
+  nd.err = e;
+  if (e == cudaSuccess) {
+    nd.scratch = static_cast<unsigned char *>(ptr);
+    nd.resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  }
+}
+
+template <int NSLOT>
+fsdp_status_t noalloc_launch(const WorkItem *items, int64_t n_items, uint32_t *status, int64_t grid,
+                             const void *const *ptrs, int n_ptrs, cudaStream_t stream) {
+  LaunchArgs<NSLOT> a;
+  a.items = items;
+  a.n_items = n_items;
+  a.status = status;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  a.fault = 0;
+  a.reserved = 0;
+  for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
+  for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *args[] = {&a};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<NSLOT>), args);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  clear_error();
+  return FSDP_OK;
+}
+
 }  // namespace
 
 fsdp_status_t device_setup(fsdp_layout *L) {
@@ -618,6 +693,58 @@ fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream) {
     return fail(FSDP_ETIMEOUT, "a bounded device wait gave up (status bits " + std::to_string(word) + ")");
   clear_error();
   return FSDP_OK;
+}
+
+fsdp_status_t fsdp_pack_reduce_scatter_noalloc(const fsdp_layout_t *L, const void *const *grads,
+                                               void *const *bucket_bufs, fsdp_stream_t stream) {
+  if (!L) return fail(FSDP_EINVAL, "layout is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FSDP_EUNSUPPORTED, "device ordinal above 63");
+  if (L->device >= 0 && L->device != dev)
+    return fail(FSDP_EINVAL, "current device is not the layout's device");
+  const int P = (int)L->desc.size(), B = (int)L->bucket.size();
+  if (P > 0 && !grads) return fail(FSDP_EINVAL, "grads is NULL");
+  if (B > 0 && !bucket_bufs) return fail(FSDP_EINVAL, "bucket_bufs is NULL");
+  fsdp_status_t st;
+  for (int p = 0; p < P; ++p) {
+    const int64_t sz = dtype_bytes(L->desc[p].grad_dtype);
+    if ((st = check_ptr(grads[p], L->desc[p].numel * sz, sz, "grads", p)) != FSDP_OK) return st;
+  }
+  for (int b = 0; b < B; ++b) {
+    const int64_t sz = dtype_bytes(L->bucket[b].dtype);
+    if ((st = check_ptr(bucket_bufs[b], (int64_t)L->W * L->bucket[b].S * sz, sz, "bucket_bufs", b)) != FSDP_OK)
+      return st;
+  }
+  const int64_t count = L->op[OP_PACK].count;
+  if (count > kNoAllocMaxItems)
+    return fail(FSDP_EUNSUPPORTED, "the pack needs " + std::to_string(count) +
+                                       " work items; the no-alloc scratch holds at most " +
+                                       std::to_string(kNoAllocMaxItems));
+  NoAllocDevice &nd = g_noalloc_devices[dev];
+  std::call_once(nd.once, noalloc_setup, std::ref(nd), dev);
+  if (nd.err != cudaSuccess)
+    return fail(FSDP_ECUDA, std::string("no-alloc scratch set-up: ") + cudaGetErrorString(nd.err));
+  if (count == 0) {
+    clear_error();
+    return FSDP_OK;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t *status = reinterpret_cast<uint32_t *>(nd.scratch);
+  WorkItem *table = reinterpret_cast<WorkItem *>(nd.scratch + kNoAllocTableOffset);
+  e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(table, L->items.data() + L->op[OP_PACK].first, (size_t)count * sizeof(WorkItem),
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("work table copy: ") + cudaGetErrorString(e));
+  const int64_t grid = count < nd.resident ? count : nd.resident;
+  const void *ptrs[kSlotsLarge];
+  for (int p = 0; p < P; ++p) ptrs[p] = grads[p];
+  for (int b = 0; b < B; ++b) ptrs[P + b] = bucket_bufs[b];
+  if (P + B <= kSlotsSmall) return noalloc_launch<kSlotsSmall>(table, count, status, grid, ptrs, P + B, s);
+  if (P + B <= kSlotsMedium) return noalloc_launch<kSlotsMedium>(table, count, status, grid, ptrs, P + B, s);
+  return noalloc_launch<kSlotsLarge>(table, count, status, grid, ptrs, P + B, s);
 }
 
 void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns) {

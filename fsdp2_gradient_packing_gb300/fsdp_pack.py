@@ -79,6 +79,7 @@ _SIGNATURES = {
     "fsdp_pack_reduce_scatter": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_allgather_copy_in": (_ST, [_LAYOUT, ctypes.POINTER(_P), _P, _P]),
     "fsdp_allgather_copy_out": (_ST, [_LAYOUT, _P, ctypes.POINTER(_P), _P]),
+    "fsdp_pack_reduce_scatter_noalloc": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_sync_status": (_ST, [_LAYOUT, _P]),
     "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
     "fsdp_layout_destroy": (None, [_LAYOUT]),
@@ -231,6 +232,12 @@ def fsdp_allgather_copy_in(layout: Layout, local_shards, ag_input, stream=None) 
 def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None) -> None:
     _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), pointer_array(full_params),
                                         _stream(stream)), "fsdp_allgather_copy_out")
+
+
+def fsdp_pack_reduce_scatter_noalloc(layout: Layout, grads, bucket_bufs, stream=None) -> None:
+    """The pack with its scratch in the library's static array (no allocation)."""
+    _check(_lib.fsdp_pack_reduce_scatter_noalloc(layout.handle, pointer_array(grads), pointer_array(bucket_bufs),
+                                                 _stream(stream)), "fsdp_pack_reduce_scatter_noalloc")
 
 
 def fsdp_sync_status(layout: Layout, stream=None) -> None:

@@ -219,6 +219,38 @@ fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_out
                                       void *const *full_params, fsdp_stream_t stream);
 
 /*
+ * Reduce-scatter copy-in without any allocation.  The pages have no
+ * counterpart: this is an extra entry point for callers that cannot allocate
+ * device memory where they pack -- code that runs while another component
+ * owns the whole device memory budget, code inside an allocator or memory-pool
+ * callback (a cudaMalloc there would re-enter the allocator), and runtimes that
+ * forbid device allocation after start-up.
+ *
+ * Same result as fsdp_pack_reduce_scatter on the same arguments.  The kernel's
+ * scratch (a status word and the work table it walks) lives in a 4 MiB array
+ * inside the library instead of memory from fsdp_plan_layout; every GPU that
+ * loads the library holds that array until the process exits.
+ *   L:  a layout from fsdp_plan_layout_host (planned without any CUDA call) or
+ *       from fsdp_plan_layout; its pack table may hold at most 131,064 work
+ *       items, else FSDP_EUNSUPPORTED and nothing is launched.  (The 50.3M
+ *       element group at W = 8 needs 12,352; items are runs of at most 8 KiB
+ *       of source and 16 KiB of destination.)
+ *   grads, bucket_bufs, stream: as for fsdp_pack_reduce_scatter.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call
+ * on a device looks up the array's device address and the grid size for that
+ * device (cudaGetSymbolAddress, device queries); make that first call before
+ * any stream capture.  Each call copies the work table into the array with
+ * cudaMemcpyAsync from the layout's host memory and clears the status word
+ * there.  Every call shares the one array: calls whose work overlaps on the
+ * GPU (on different streams, or from different threads) race and corrupt
+ * each other's tables; order them on one stream.  A bounded device wait that
+ * gives up in this variant records its status bit in the array and is not
+ * read back.
+ */
+fsdp_status_t fsdp_pack_reduce_scatter_noalloc(const fsdp_layout_t *L, const void *const *grads,
+                                               void *const *bucket_bufs, fsdp_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the layout's device status word.
  * Every wait inside the kernels is bounded; a wait that gives up (which only
  * a broken pipeline could cause) records a bit there and its thread leaves
