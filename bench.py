@@ -58,9 +58,24 @@ METRIC = "reduce-scatter pack GB/s and ms per fully_shard (50.3M elem, W=8) vs H
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 ESZ = {"f32": 4, "bf16": 2}
-WORKLOAD = ("mixed50m_W8: one fully_shard group of 4 layers at d=1024 (50,331,648 BF16 + 8,192 FP32 "
-            "gradients), W=8, reduce FP32, shards FP32, params BF16 matrices / FP32 norms; "
-            "step = reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out")
+STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
+WORKLOADS = {
+    # name: (factory, description); the first is the benchmark's workload.
+    "mixed50m": (lambda: wl.mixed_50m(W=8),
+                 "mixed50m_W8: one fully_shard group of 4 layers at d=1024 (50,331,648 BF16 + 8,192 FP32 "
+                 "gradients), W=8, reduce FP32, shards FP32, params BF16 matrices / FP32 norms"),
+    "transformer500": (lambda: wl.transformer_500(W=8),
+                       "transformer500_W8: 24 fully_shard groups (one per layer, d=512, 17 tensors each, "
+                       "408 in all), W=8, reduce FP32, shards FP32, params BF16 matrices / FP32 small"),
+    "kda_w8": (lambda: wl.kda_block(W=8, reduce="f32"),
+               "kda_block_W8: one KDA-style block at d=4096 (218,116,128 parameters), W=8, reduce FP32"),
+    "kda_w64": (lambda: wl.kda_block(W=64, reduce="f32"),
+                "kda_block_W64: one KDA-style block at d=4096 (218,116,128 parameters), W=64 (odd row "
+                "length: every row misaligned), reduce FP32"),
+    "kda_w8_grad": (lambda: wl.kda_block(W=8, reduce="grad"),
+                    "kda_block_W8_two_buckets: one KDA-style block, W=8, reduce dtype = gradient dtype "
+                    "(BF16 and FP32 buckets)"),
+}
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pack_mixed50m_w8_ncu.md")
 
 
@@ -73,6 +88,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed50m",
+                    help="layout to time (the benchmark's metric is quoted on mixed50m)")
     return ap.parse_args(argv)
 
 
@@ -231,11 +248,12 @@ def flat_offsets(sizes, align=256):
     return offs, max(at, align)
 
 
-def host_inputs(work, W):
-    specs = work.groups[0]
+def host_inputs(work, g):
+    """Seeded gradients and every rank's shards of group g."""
+    specs, W = work.groups[g], work.W
     c = chunks(specs, W)
-    grads = [wl.grad_values(work, 0, i) for i in range(len(specs))]
-    shards = [[wl.shard_values(work, 0, i, r, c[i], max(0, min(c[i], s.numel - r * c[i])))
+    grads = [wl.grad_values(work, g, i) for i in range(len(specs))]
+    shards = [[wl.shard_values(work, g, i, r, c[i], max(0, min(c[i], s.numel - r * c[i])))
                for i, s in enumerate(specs)] for r in range(W)]
     return grads, shards
 
@@ -252,53 +270,56 @@ def flatten(arrays, offs, total):
 # The CPU oracle on bounded samples: one (rank, parameter) run at a time.
 # ---------------------------------------------------------------------------
 class OracleSampler:
-    """Cycles through the segments of one step of the path (pack runs,
-    copy-in runs of rank 0, copy-out runs), each with its algorithmic bytes."""
+    """Cycles through the segments of one step of the path over every group
+    (pack runs, copy-in runs of rank 0, copy-out runs), each with its
+    algorithmic bytes."""
 
-    def __init__(self, work, W, grads, shards):
+    def __init__(self, work, inputs):
         import oracle
         self.oracle = oracle
-        specs = work.groups[0]
-        self.pl = pl = oracle.plan(oracle.params_from_specs(specs), W)
-        self.grads, self.shards0 = grads, shards[0]
-        self.bufs = [np.empty(W * S, oracle.DTYPE_NP[d]) for d, S in zip(pl.bucket_dtype, pl.bucket_S)]
-        self.row = np.empty(pl.S_ag, np.uint8)
-        rows = [oracle.allgather_copy_in(pl, shards[r]) for r in range(W)]
-        self.gathered = np.concatenate(rows)
-        self.full = [np.empty(s.numel, oracle.DTYPE_NP[p.param_dtype]) for s, p in zip(specs, pl.params)]
-        segs = []
-        for b in range(len(pl.bucket_dtype)):
-            for r in range(W):
-                for p, prm in enumerate(pl.params):
-                    if pl.bucket_of[p] != b:
-                        continue
+        W = work.W
+        self.segs = []
+        for g, specs in enumerate(work.groups):
+            grads, shards = inputs[g]
+            pl = oracle.plan(oracle.params_from_specs(specs), W)
+            st = {
+                "pl": pl, "grads": grads, "shards0": shards[0],
+                "bufs": [np.empty(W * S, oracle.DTYPE_NP[d]) for d, S in zip(pl.bucket_dtype, pl.bucket_S)],
+                "row": np.empty(pl.S_ag, np.uint8),
+                "gathered": np.concatenate([oracle.allgather_copy_in(pl, shards[r]) for r in range(W)]),
+                "full": [np.empty(p.numel, oracle.DTYPE_NP[p.param_dtype]) for p in pl.params],
+            }
+            sz = oracle.DTYPE_SIZE
+            for b in range(len(pl.bucket_dtype)):
+                for r in range(W):
+                    for p, prm in enumerate(pl.params):
+                        if pl.bucket_of[p] != b:
+                            continue
+                        valid = max(0, min(pl.chunk[p], prm.numel - r * pl.chunk[p]))
+                        nbytes = valid * sz[prm.grad_dtype] + pl.chunk[p] * sz[pl.bucket_dtype[b]]
+                        self.segs.append((self._pack, (st, r, p), nbytes))
+            gap = pl.S_ag - sum(c * sz[p.param_dtype] for c, p in zip(pl.chunk, pl.params))
+            self.segs.append((self._clear, (st,), gap))
+            for p, prm in enumerate(pl.params):
+                self.segs.append((self._copy_in, (st, p), pl.chunk[p] * (sz[prm.shard_dtype] + sz[prm.param_dtype])))
+            for p, prm in enumerate(pl.params):
+                for r in range(W):
                     valid = max(0, min(pl.chunk[p], prm.numel - r * pl.chunk[p]))
-                    nbytes = valid * oracle.DTYPE_SIZE[prm.grad_dtype] + pl.chunk[p] * oracle.DTYPE_SIZE[pl.bucket_dtype[b]]
-                    segs.append((self._pack, (r, p), nbytes))
-        gap = pl.S_ag - sum(c * oracle.DTYPE_SIZE[p.param_dtype] for c, p in zip(pl.chunk, pl.params))
-        segs.append((self._clear, (), gap))
-        for p, prm in enumerate(pl.params):
-            nbytes = pl.chunk[p] * (oracle.DTYPE_SIZE[prm.shard_dtype] + oracle.DTYPE_SIZE[prm.param_dtype])
-            segs.append((self._copy_in, (p,), nbytes))
-        for p, prm in enumerate(pl.params):
-            for r in range(W):
-                valid = max(0, min(pl.chunk[p], prm.numel - r * pl.chunk[p]))
-                segs.append((self._copy_out, (p, r), 2 * valid * oracle.DTYPE_SIZE[prm.param_dtype]))
-        self.segs = segs
-        self.step_bytes = sum(s[2] for s in segs)
+                    self.segs.append((self._copy_out, (st, p, r), 2 * valid * sz[prm.param_dtype]))
+        self.step_bytes = sum(s[2] for s in self.segs)
         self.i = 0
 
-    def _pack(self, r, p):
-        self.oracle.pack_segment(self.pl, self.grads, self.bufs, r, p)
+    def _pack(self, st, r, p):
+        self.oracle.pack_segment(st["pl"], st["grads"], st["bufs"], r, p)
 
-    def _clear(self):
-        self.oracle.allgather_copy_in_clear(self.pl, self.row)
+    def _clear(self, st):
+        self.oracle.allgather_copy_in_clear(st["pl"], st["row"])
 
-    def _copy_in(self, p):
-        self.oracle.allgather_copy_in_segment(self.pl, self.shards0, self.row, p)
+    def _copy_in(self, st, p):
+        self.oracle.allgather_copy_in_segment(st["pl"], st["shards0"], st["row"], p)
 
-    def _copy_out(self, p, r):
-        self.oracle.allgather_copy_out_segment(self.pl, self.gathered, self.full, p, r)
+    def _copy_out(self, st, p, r):
+        self.oracle.allgather_copy_out_segment(st["pl"], st["gathered"], st["full"], p, r)
 
     def next(self) -> int:
         fn, args, nbytes = self.segs[self.i]
@@ -375,6 +396,25 @@ class DeviceSet:
             ev[3].record()
 
 
+class Group:
+    """One fully_shard group on the device: its layout and two buffer sets."""
+
+    def __init__(self, fp, torch, work, g, inputs):
+        self.specs = work.groups[g]
+        self.L = fp.fsdp_plan_layout(self.specs, work.W)
+        self.info = fp.fsdp_layout_query(self.L)
+        bucket_bytes = [fp.fsdp_layout_bucket(self.L, b).bytes for b in range(self.info.n_buckets)]
+        self.nbytes = op_bytes(self.specs, work.W, bucket_bytes, self.info.ag_bytes)
+        grads, shards = inputs
+        self.sets = [DeviceSet(fp, torch, self.L, self.specs, work.W, self.info, grads, shards, 0) for _ in range(2)]
+
+
+def run_steps(fp, groups, h, first, count, evs=None):
+    for i in range(first, first + count):
+        for gi, grp in enumerate(groups):
+            grp.sets[i & 1].step(fp, grp.L, h, None if evs is None else evs[i - first][gi])
+
+
 def run_ours(args):
     import torch
     from fsdp2_gradient_packing_gb300 import _build
@@ -384,22 +424,16 @@ def run_ours(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     init_dist("nccl" if world > 1 else "gloo")
-    W = 8
-    work = wl.mixed_50m(W=W)
-    specs = work.groups[0]
-    host_grads, host_shards = host_inputs(work, W)
-    L = fp.fsdp_plan_layout(specs, W)
-    info = fp.fsdp_layout_query(L)
-    bucket_bytes = [fp.fsdp_layout_bucket(L, b).bytes for b in range(info.n_buckets)]
-    nbytes = op_bytes(specs, W, bucket_bytes, info.ag_bytes)
+    factory, description = WORKLOADS[args.workload]
+    work = factory()
+    inputs = [host_inputs(work, g) for g in range(len(work.groups))]
+    groups = [Group(fp, torch, work, g, inputs[g]) for g in range(len(work.groups))]
+    nbytes = {k: sum(grp.nbytes[k] for grp in groups) for k in ("pack", "copy_in", "copy_out")}
     step_bytes = sum(nbytes.values())
-
-    sets = [DeviceSet(fp, torch, L, specs, W, info, host_grads, host_shards, 0) for _ in range(2)]
-    stream = torch.cuda.current_stream()
-    h = stream.cuda_stream
-    for i in range(args.warmup):
-        sets[i & 1].step(fp, L, h)
-    fp.fsdp_sync_status(L)
+    h = torch.cuda.current_stream().cuda_stream
+    run_steps(fp, groups, h, 0, args.warmup)
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
 
     K = args.steps
     gpu_id = None
@@ -416,67 +450,74 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first sample before the load starts
     t_start.record()
-    for i in range(K):
-        sets[i & 1].step(fp, L, h)
+    run_steps(fp, groups, h, 0, K)
     t_end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     barrier()
-    fp.fsdp_sync_status(L)
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), device=torch.device("cuda"))
 
     # Pass 2: the same K steps with a CUDA event around every launch, for the
     # per-operation device times (events between launches serialise them).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in groups] for _ in range(K)]
     torch.cuda.synchronize()
     barrier()
-    for i in range(K):
-        sets[i & 1].step(fp, L, h, evs[i])
+    run_steps(fp, groups, h, 0, K, evs)
     torch.cuda.synchronize()
     barrier()
-    fp.fsdp_sync_status(L)
-    per = {k: [e[j].elapsed_time(e[j + 1]) for e in evs] for j, k in enumerate(("pack", "copy_in", "copy_out"))}
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
+    per = {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs]
+           for j, k in enumerate(("pack", "copy_in", "copy_out"))}
 
     # End to end through the same API with host buffers: every step copies
     # its inputs from pinned host memory and reads its results back.
-    s0 = sets[0]
-    pin = lambda t: torch.empty(t.numel(), dtype=torch.uint8, pin_memory=True)  # noqa: E731
-    h_grads, h_shards = pin(s0.grads), pin(s0.shards)
-    h_grads.copy_(s0.grads.cpu())
-    h_shards.copy_(s0.shards.cpu())
-    others = torch.cat([s0.gathered[:0], s0.gathered[s0.S_ag:]])  # rows 1..W-1
-    h_others = pin(others)
-    h_others.copy_(others.cpu())
-    h_buckets = [pin(b) for b in s0.buckets]
-    h_full = pin(s0.full)
-    h2d = h_grads.numel() + h_shards.numel() + h_others.numel()
-    d2h = sum(b.numel() for b in h_buckets) + h_full.numel()
+    pin = lambda n: torch.empty(n, dtype=torch.uint8, pin_memory=True)  # noqa: E731
+    host = []
+    for grp in groups:
+        s0 = grp.sets[0]
+        hb = {"grads": pin(s0.grads.numel()), "shards": pin(s0.shards.numel()),
+              "others": pin(s0.gathered.numel() - s0.S_ag),
+              "buckets": [pin(b.numel()) for b in s0.buckets], "full": pin(s0.full.numel())}
+        hb["grads"].copy_(s0.grads.cpu())
+        hb["shards"].copy_(s0.shards.cpu())
+        hb["others"].copy_(s0.gathered[s0.S_ag:].cpu())
+        host.append(hb)
+    h2d = sum(hb["grads"].numel() + hb["shards"].numel() + hb["others"].numel() for hb in host)
+    d2h = sum(sum(b.numel() for b in hb["buckets"]) + hb["full"].numel() for hb in host)
     E = max(3, args.e2e_steps)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier()
     e_start.record()
     for _ in range(E):
-        s0.grads.copy_(h_grads, non_blocking=True)
-        s0.shards.copy_(h_shards, non_blocking=True)
-        s0.gathered[s0.S_ag:].copy_(h_others, non_blocking=True)
-        s0.step(fp, L, h)
-        for hb, db in zip(h_buckets, s0.buckets):
-            hb.copy_(db, non_blocking=True)
-        h_full.copy_(s0.full, non_blocking=True)
+        for grp, hb in zip(groups, host):
+            s0 = grp.sets[0]
+            s0.grads.copy_(hb["grads"], non_blocking=True)
+            s0.shards.copy_(hb["shards"], non_blocking=True)
+            s0.gathered[s0.S_ag:].copy_(hb["others"], non_blocking=True)
+            s0.step(fp, grp.L, h)
+            for hbuf, dbuf in zip(hb["buckets"], s0.buckets):
+                hbuf.copy_(dbuf, non_blocking=True)
+            hb["full"].copy_(s0.full, non_blocking=True)
     e_end.record()
     torch.cuda.synchronize()
     barrier()
-    fp.fsdp_sync_status(L)
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device=torch.device("cuda"))
 
     result = None
+    n_launch = len(groups)
     if rank == 0:
         peak, peak_kind = read_peaks()
         pack_ms = statistics.mean(per["pack"])
         achieved = nbytes["pack"] / (pack_ms * 1e-3) / 1e9
-        rows = {k: {"bytes": nbytes[k], "ms_mean": statistics.mean(v), "ms_median": statistics.median(v),
-                    "ms_min": min(v), "gbs": nbytes[k] / (statistics.mean(v) * 1e-3) / 1e9}
+        rows = {k: {"bytes": nbytes[k], "launches_per_step": n_launch, "ms_mean": statistics.mean(v),
+                    "ms_median": statistics.median(v), "ms_min": min(v),
+                    "gbs": nbytes[k] / (statistics.mean(v) * 1e-3) / 1e9}
                 for k, v in per.items()}
         result = {
             "metric": METRIC,
@@ -491,25 +532,28 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "bf16+f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "world_size_layout": W, "step_bytes": step_bytes,
+            "config": {"workload": f"{description}; {STEP}", "world_size_layout": work.W,
+                       "groups": len(groups), "step_bytes": step_bytes,
                        "parallelism": f"replicas x{world} (no data-path collective)",
-                       "l2": "inputs larger than L2: two rotating buffer sets, 1.06 GB per step pair "
-                             "vs 129 MB L2; no flush"},
+                       "l2": "inputs larger than L2: two rotating buffer sets of "
+                             f"{2 * step_bytes / 1e9:.2f} GB of algorithmic traffic vs 129 MB L2; no flush"},
             "ops": rows,
             "ops_note": "per-operation device times from a second pass of the same K steps with CUDA "
-                        "events around every launch",
-            "roofline": {"bound": "hbm", "kernel": "walk_kernel (reduce-scatter pack launch)",
+                        "events around every launch (summed over the step's groups)",
+            "roofline": {"bound": "hbm", "kernel": "walk_kernel (reduce-scatter pack launches)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": f"{peak_kind} hbm_gbs (burst copy)" if peak_kind == "measured" else "fallback",
-                         "bytes_per_launch": nbytes["pack"], "traffic": read_traffic()},
+                         "bytes_per_launch": nbytes["pack"] / n_launch,
+                         "traffic": read_traffic() if args.workload == "mixed50m" else None},
             "e2e": {"value": world * step_bytes * E / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E},
-            "gpu_launches": 3 * K,
+            "gpu_launches": 3 * n_launch * K,
             "clocks": clocks,
         }
-    L.close()
+    for grp in groups:
+        grp.L.close()
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        samp = OracleSampler(work, W, host_grads, host_shards)
+        samp = OracleSampler(work, inputs)
         result["cpu_baseline"] = cpu_baseline(samp, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -525,10 +569,10 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    W = 8
-    work = wl.mixed_50m(W=W)
-    host_grads, host_shards = host_inputs(work, W)
-    samp = OracleSampler(work, W, host_grads, host_shards)
+    factory, description = WORKLOADS[args.workload]
+    work = factory()
+    inputs = [host_inputs(work, g) for g in range(len(work.groups))]
+    samp = OracleSampler(work, inputs)
     for _ in range(args.warmup):
         samp.next()
     done = 0
@@ -542,8 +586,8 @@ def run_reference(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "world_size_layout": W, "step_bytes": samp.step_bytes,
-                   "parallelism": "single host thread"},
+        "config": {"workload": f"{description}; {STEP}", "world_size_layout": work.W,
+                   "groups": len(work.groups), "step_bytes": samp.step_bytes, "parallelism": "single host thread"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "each step = one (rank, parameter) run of the pack, copy-in or copy-out, "
                                    f"cycling through the {len(samp.segs)} runs of a whole step"},
