@@ -90,6 +90,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed50m",
                     help="layout to time (the benchmark's metric is quoted on mixed50m)")
+    ap.add_argument("--batched", action="store_true",
+                    help="one launch per operation for all of the workload's groups (*_batched entry points)")
     return ap.parse_args(argv)
 
 
@@ -409,8 +411,41 @@ class Group:
         self.sets = [DeviceSet(fp, torch, self.L, self.specs, work.W, self.info, grads, shards, 0) for _ in range(2)]
 
 
-def run_steps(fp, groups, h, first, count, evs=None):
+class Batch:
+    """The pointer arrays of the batched entry points for both buffer sets."""
+
+    def __init__(self, fp, groups):
+        self.layouts = fp.layout_array([grp.L for grp in groups])
+        self.n = len(groups)
+        cat = lambda arrs: fp.pointer_array([p for a in arrs for p in a])  # noqa: E731
+        self.sets = []
+        for k in range(2):
+            ss = [grp.sets[k] for grp in groups]
+            self.sets.append(dict(
+                grads=cat(s.grad_ptrs for s in ss), buckets=cat(s.bucket_ptrs for s in ss),
+                shards=cat(s.shard_ptrs for s in ss), rows=fp.pointer_array([s.row_ptr for s in ss]),
+                gathered=fp.pointer_array([s.gathered.data_ptr() for s in ss]), full=cat(s.full_ptrs for s in ss)))
+
+    def step(self, fp, h, k, ev=None):
+        a = self.sets[k]
+        if ev is not None:
+            ev[0].record()
+        fp.fsdp_pack_reduce_scatter_batched(self.layouts, a["grads"], a["buckets"], h)
+        if ev is not None:
+            ev[1].record()
+        fp.fsdp_allgather_copy_in_batched(self.layouts, a["shards"], a["rows"], h)
+        if ev is not None:
+            ev[2].record()
+        fp.fsdp_allgather_copy_out_batched(self.layouts, a["gathered"], a["full"], h)
+        if ev is not None:
+            ev[3].record()
+
+
+def run_steps(fp, groups, h, first, count, evs=None, batch=None):
     for i in range(first, first + count):
+        if batch is not None:
+            batch.step(fp, h, i & 1, None if evs is None else evs[i - first][0])
+            continue
         for gi, grp in enumerate(groups):
             grp.sets[i & 1].step(fp, grp.L, h, None if evs is None else evs[i - first][gi])
 
@@ -431,7 +466,9 @@ def run_ours(args):
     nbytes = {k: sum(grp.nbytes[k] for grp in groups) for k in ("pack", "copy_in", "copy_out")}
     step_bytes = sum(nbytes.values())
     h = torch.cuda.current_stream().cuda_stream
-    run_steps(fp, groups, h, 0, args.warmup)
+    batch = Batch(fp, groups) if args.batched else None
+    n_launch = 1 if batch is not None else len(groups)
+    run_steps(fp, groups, h, 0, args.warmup, batch=batch)
     for grp in groups:
         fp.fsdp_sync_status(grp.L)
 
@@ -450,7 +487,7 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first sample before the load starts
     t_start.record()
-    run_steps(fp, groups, h, 0, K)
+    run_steps(fp, groups, h, 0, K, batch=batch)
     t_end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -461,10 +498,10 @@ def run_ours(args):
 
     # Pass 2: the same K steps with a CUDA event around every launch, for the
     # per-operation device times (events between launches serialise them).
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in groups] for _ in range(K)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_launch)] for _ in range(K)]
     torch.cuda.synchronize()
     barrier()
-    run_steps(fp, groups, h, 0, K, evs)
+    run_steps(fp, groups, h, 0, K, evs, batch=batch)
     torch.cuda.synchronize()
     barrier()
     for grp in groups:
@@ -510,7 +547,6 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device=torch.device("cuda"))
 
     result = None
-    n_launch = len(groups)
     if rank == 0:
         peak, peak_kind = read_peaks()
         pack_ms = statistics.mean(per["pack"])
@@ -533,7 +569,7 @@ def run_ours(args):
             "dtype": "bf16+f32",
             "data": "synthetic",
             "config": {"workload": f"{description}; {STEP}", "world_size_layout": work.W,
-                       "groups": len(groups), "step_bytes": step_bytes,
+                       "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
                        "parallelism": f"replicas x{world} (no data-path collective)",
                        "l2": "inputs larger than L2: two rotating buffer sets of "
                              f"{2 * step_bytes / 1e9:.2f} GB of algorithmic traffic vs 129 MB L2; no flush"},

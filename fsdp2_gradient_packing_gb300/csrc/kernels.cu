@@ -68,6 +68,8 @@ constexpr int32_t kFaultSkipFirstStage = 1;
 
 // Per-call pointers travel by value in the parameter block: `slot` is read
 // with a run-time index, which __grid_constant__ allows without a local copy.
+// fetch(i) returns work item i and the slot base its slot numbers are
+// relative to.
 template <int NSLOT>
 struct LaunchArgs {
   const WorkItem *items;
@@ -77,6 +79,38 @@ struct LaunchArgs {
   int32_t fault;
   int32_t reserved;
   const void *slot[NSLOT];
+
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base) const {
+    *base = 0;
+    return items[i];
+  }
+};
+
+// Several layouts in one launch: the items of layout g are global items
+// [start[g], start[g+1]); their slots are numbered from slot_base[g].
+constexpr int kMaxBatch = 64;
+template <int NSLOT>
+struct BatchArgs {
+  int64_t n_items;
+  uint32_t *status;
+  uint64_t wait_limit_ns;
+  int32_t fault;
+  int32_t n_groups;
+  const WorkItem *items[kMaxBatch];
+  int64_t start[kMaxBatch + 1];
+  int32_t slot_base[kMaxBatch];
+  const void *slot[NSLOT];
+
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base) const {
+    int lo = 0, hi = n_groups - 1;  // the last group that starts at or before i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (start[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    *base = slot_base[lo];
+    return items[lo][i - start[lo]];
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -323,8 +357,8 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
   }
 }
 
-template <int NSLOT>
-__global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant__ LaunchArgs<NSLOT> a) {
+template <class Args>
+__global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageStride);
   uint64_t *empty = full + kStages;
@@ -347,11 +381,13 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     bool skipped_first = false;
     int64_t i = blockIdx.x;
     WorkItem next{};
-    if (i < a.n_items) next = a.items[i];
+    int32_t next_base = 0;
+    if (i < a.n_items) next = a.fetch(i, &next_base);
     wait_for_previous_grid();
     for (; i < a.n_items; i += gridDim.x, ++k) {
       const WorkItem w = next;
-      if (i + gridDim.x < a.n_items) next = a.items[i + gridDim.x];
+      const int32_t base = next_base;
+      if (i + gridDim.x < a.n_items) next = a.fetch(i + gridDim.x, &next_base);
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
@@ -363,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         continue;
       }
       const int ss = (w.kind & 1) ? 2 : 4, ds = (w.kind & 2) ? 2 : 4;
-      const char *src = reinterpret_cast<const char *>(a.slot[w.src_slot]) + w.src_off * (int64_t)ss;
+      const char *src = reinterpret_cast<const char *>(a.slot[base + w.src_slot]) + w.src_off * (int64_t)ss;
       const Interior in = interior_of(src, w.n_copy * ss);
       uint32_t bytes = (uint32_t)(in.hi - in.lo);
       StageHeader *hd = reinterpret_cast<StageHeader *>(smem + s * kStageStride);
       hd->src = src;
-      hd->dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[w.dst_slot])) + w.dst_off * (int64_t)ds;
+      hd->dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[base + w.dst_slot])) + w.dst_off * (int64_t)ds;
       hd->n_copy = w.n_copy;
       hd->n_total = w.n_total;
       hd->kind = w.kind;
@@ -450,7 +486,7 @@ fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptr
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *args[] = {&a};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<NSLOT>), args);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<LaunchArgs<NSLOT>>), args);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
   clear_error();
   return FSDP_OK;
@@ -464,6 +500,63 @@ fsdp_status_t launch(const fsdp_layout *L, Op op, const void *const *ptrs, int n
   if (n_ptrs <= kSlotsSmall) return launch_variant<kSlotsSmall>(L, op, ptrs, n_ptrs, stream);
   if (n_ptrs <= kSlotsMedium) return launch_variant<kSlotsMedium>(L, op, ptrs, n_ptrs, stream);
   return launch_variant<kSlotsLarge>(L, op, ptrs, n_ptrs, stream);
+}
+
+// Several layouts' work in one launch (the *_batched entry points).  The
+// largest variant leaves room for the per-layout table in the parameter block.
+constexpr int kBatchSlotsLarge = 3840;
+static_assert(sizeof(BatchArgs<kBatchSlotsLarge>) <= 32764, "batched parameter block too large");
+
+template <int NSLOT>
+fsdp_status_t batch_launch_variant(const fsdp_layout *const *Ls, int n, Op op, const void *const *ptrs, int n_ptrs,
+                                   const int32_t *slot_base, cudaStream_t stream) {
+  BatchArgs<NSLOT> a;
+  int64_t total = 0;
+  int groups = 0;
+  for (int g = 0; g < n; ++g) {
+    const int64_t c = Ls[g]->op[op].count;
+    if (c == 0) continue;
+    a.items[groups] = Ls[g]->d_items + Ls[g]->op[op].first;
+    a.start[groups] = total;
+    a.slot_base[groups] = slot_base[g];
+    total += c;
+    ++groups;
+  }
+  if (total == 0) {
+    clear_error();
+    return FSDP_OK;
+  }
+  a.start[groups] = total;
+  a.n_groups = groups;
+  a.n_items = total;
+  a.status = Ls[0]->d_status;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  a.fault = g_fault.load(std::memory_order_relaxed);
+  for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
+  for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
+  const int64_t grid = total < Ls[0]->resident ? total : Ls[0]->resident;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *args[] = {&a};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<BatchArgs<NSLOT>>), args);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  clear_error();
+  return FSDP_OK;
+}
+
+fsdp_status_t batch_launch(const fsdp_layout *const *Ls, int n, Op op, const void *const *ptrs, int n_ptrs,
+                           const int32_t *slot_base, cudaStream_t stream) {
+  if (n_ptrs <= kSlotsSmall) return batch_launch_variant<kSlotsSmall>(Ls, n, op, ptrs, n_ptrs, slot_base, stream);
+  if (n_ptrs <= kSlotsMedium) return batch_launch_variant<kSlotsMedium>(Ls, n, op, ptrs, n_ptrs, slot_base, stream);
+  return batch_launch_variant<kBatchSlotsLarge>(Ls, n, op, ptrs, n_ptrs, slot_base, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -492,7 +585,7 @@ fsdp_status_t check_ptr(const void *p, int64_t bytes, int64_t align, const char 
 
 template <int NSLOT>
 cudaError_t allow_smem() {
-  return cudaFuncSetAttribute(reinterpret_cast<const void *>(&walk_kernel<NSLOT>),
+  return cudaFuncSetAttribute(reinterpret_cast<const void *>(&walk_kernel<LaunchArgs<NSLOT>>),
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
@@ -533,7 +626,7 @@ void noalloc_setup(NoAllocDevice &nd, int dev) {
   cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<kSlotsSmall>, kThreads, kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<LaunchArgs<kSlotsSmall>>, kThreads, kSmemBytes);
   nd.err = e;
   if (e == cudaSuccess) {
     nd.scratch = static_cast<unsigned char *>(ptr);
@@ -564,7 +657,7 @@ fsdp_status_t noalloc_launch(const WorkItem *items, int64_t n_items, uint32_t *s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *args[] = {&a};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<NSLOT>), args);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<LaunchArgs<NSLOT>>), args);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
   clear_error();
   return FSDP_OK;
@@ -580,9 +673,10 @@ fsdp_status_t device_setup(fsdp_layout *L) {
   if (e == cudaSuccess) e = allow_smem<kSlotsMedium>();
   if (e == cudaSuccess) e = allow_smem<kSlotsLarge>();
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<kSlotsSmall>, kThreads, kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<LaunchArgs<kSlotsSmall>>, kThreads, kSmemBytes);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("device query failed: ") + cudaGetErrorString(e));
   const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  L->resident = resident;
   for (int op = 0; op < OP_COUNT; ++op) {
     int64_t g = L->op[op].count < resident ? L->op[op].count : resident;
     L->op[op].grid = (int32_t)(g > 0 ? g : 0);
@@ -679,6 +773,109 @@ fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_out
   ptrs[0] = ag_output;
   for (int p = 0; p < P; ++p) ptrs[1 + p] = full_params[p];
   return launch(L, OP_COPY_OUT, ptrs, P + 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Batched calls: several layouts' work in one launch.
+// ---------------------------------------------------------------------------
+static fsdp_status_t check_batch(const fsdp_layout_t *const *Ls, int32_t n) {
+  if (n < 0) return fail(FSDP_EINVAL, "n_layouts < 0");
+  if (n > kMaxBatch) return fail(FSDP_EUNSUPPORTED, "more than 64 layouts in one batch");
+  if (n > 0 && !Ls) return fail(FSDP_EINVAL, "layouts is NULL");
+  for (int32_t g = 0; g < n; ++g) {
+    fsdp_status_t st = check_layout(Ls[g]);
+    if (st != FSDP_OK) return st;
+  }
+  return FSDP_OK;
+}
+
+fsdp_status_t fsdp_pack_reduce_scatter_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                               const void *const *grads, void *const *bucket_bufs,
+                                               fsdp_stream_t stream) {
+  fsdp_status_t st = check_batch(layouts, n_layouts);
+  if (st != FSDP_OK) return st;
+  int64_t slots = 0, n_grads = 0, n_bufs = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) {
+    n_grads += (int64_t)layouts[g]->desc.size();
+    n_bufs += (int64_t)layouts[g]->bucket.size();
+  }
+  slots = n_grads + n_bufs;
+  if (slots > kBatchSlotsLarge) return fail(FSDP_EUNSUPPORTED, "more than 3840 pointers in one batch");
+  if (n_grads > 0 && !grads) return fail(FSDP_EINVAL, "grads is NULL");
+  if (n_bufs > 0 && !bucket_bufs) return fail(FSDP_EINVAL, "bucket_bufs is NULL");
+  const void *ptrs[kBatchSlotsLarge];
+  int32_t base[kMaxBatch];
+  int64_t gi = 0, bi = 0, at = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) {
+    const fsdp_layout *L = layouts[g];
+    base[g] = (int32_t)at;
+    for (size_t p = 0; p < L->desc.size(); ++p, ++gi) {
+      const int64_t sz = dtype_bytes(L->desc[p].grad_dtype);
+      if ((st = check_ptr(grads[gi], L->desc[p].numel * sz, sz, "grads", gi)) != FSDP_OK) return st;
+      ptrs[at++] = grads[gi];
+    }
+    for (size_t b = 0; b < L->bucket.size(); ++b, ++bi) {
+      const int64_t sz = dtype_bytes(L->bucket[b].dtype);
+      if ((st = check_ptr(bucket_bufs[bi], (int64_t)L->W * L->bucket[b].S * sz, sz, "bucket_bufs", bi)) != FSDP_OK)
+        return st;
+      ptrs[at++] = bucket_bufs[bi];
+    }
+  }
+  return batch_launch(layouts, n_layouts, OP_PACK, ptrs, (int)at, base, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_allgather_copy_in_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                             const void *const *local_shards, void *const *ag_inputs,
+                                             fsdp_stream_t stream) {
+  fsdp_status_t st = check_batch(layouts, n_layouts);
+  if (st != FSDP_OK) return st;
+  int64_t n_shards = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) n_shards += (int64_t)layouts[g]->desc.size();
+  if (n_shards + n_layouts > kBatchSlotsLarge) return fail(FSDP_EUNSUPPORTED, "more than 3840 pointers in one batch");
+  if (n_shards > 0 && !local_shards) return fail(FSDP_EINVAL, "local_shards is NULL");
+  if (n_layouts > 0 && !ag_inputs) return fail(FSDP_EINVAL, "ag_inputs is NULL");
+  const void *ptrs[kBatchSlotsLarge];
+  int32_t base[kMaxBatch];
+  int64_t si = 0, at = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) {
+    const fsdp_layout *L = layouts[g];
+    base[g] = (int32_t)at;
+    for (size_t p = 0; p < L->desc.size(); ++p, ++si) {
+      const int64_t sz = dtype_bytes(L->desc[p].shard_dtype);
+      if ((st = check_ptr(local_shards[si], L->param[p].chunk * sz, sz, "local_shards", si)) != FSDP_OK) return st;
+      ptrs[at++] = local_shards[si];
+    }
+    if ((st = check_ptr(ag_inputs[g], L->S_ag, 16, "ag_inputs", g)) != FSDP_OK) return st;
+    ptrs[at++] = ag_inputs[g];
+  }
+  return batch_launch(layouts, n_layouts, OP_COPY_IN, ptrs, (int)at, base, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_allgather_copy_out_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                              const void *const *ag_outputs, void *const *full_params,
+                                              fsdp_stream_t stream) {
+  fsdp_status_t st = check_batch(layouts, n_layouts);
+  if (st != FSDP_OK) return st;
+  int64_t n_params = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) n_params += (int64_t)layouts[g]->desc.size();
+  if (n_params + n_layouts > kBatchSlotsLarge) return fail(FSDP_EUNSUPPORTED, "more than 3840 pointers in one batch");
+  if (n_layouts > 0 && !ag_outputs) return fail(FSDP_EINVAL, "ag_outputs is NULL");
+  if (n_params > 0 && !full_params) return fail(FSDP_EINVAL, "full_params is NULL");
+  const void *ptrs[kBatchSlotsLarge];
+  int32_t base[kMaxBatch];
+  int64_t pi = 0, at = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) {
+    const fsdp_layout *L = layouts[g];
+    base[g] = (int32_t)at;
+    if ((st = check_ptr(ag_outputs[g], (int64_t)L->W * L->S_ag, 16, "ag_outputs", g)) != FSDP_OK) return st;
+    ptrs[at++] = ag_outputs[g];
+    for (size_t p = 0; p < L->desc.size(); ++p, ++pi) {
+      const int64_t sz = dtype_bytes(L->desc[p].param_dtype);
+      if ((st = check_ptr(full_params[pi], L->desc[p].numel * sz, sz, "full_params", pi)) != FSDP_OK) return st;
+      ptrs[at++] = full_params[pi];
+    }
+  }
+  return batch_launch(layouts, n_layouts, OP_COPY_OUT, ptrs, (int)at, base, reinterpret_cast<cudaStream_t>(stream));
 }
 
 fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream) {

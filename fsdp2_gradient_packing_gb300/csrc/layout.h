@@ -91,6 +91,7 @@ struct fsdp_layout {
   int64_t S_ag = 0;
   std::vector<fsdp::WorkItem> items;   // pack, copy-in, copy-out tables back to back
   fsdp::OpTable op[fsdp::OP_COUNT];
+  int64_t resident = 0;                // CTAs a launch keeps resident on the device
   fsdp::WorkItem *d_items = nullptr;   // device copy of `items`
   uint32_t *d_status = nullptr;        // device status word (bounded-wait failures)
 };

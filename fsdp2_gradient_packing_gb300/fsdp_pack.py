@@ -79,6 +79,12 @@ _SIGNATURES = {
     "fsdp_pack_reduce_scatter": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_allgather_copy_in": (_ST, [_LAYOUT, ctypes.POINTER(_P), _P, _P]),
     "fsdp_allgather_copy_out": (_ST, [_LAYOUT, _P, ctypes.POINTER(_P), _P]),
+    "fsdp_pack_reduce_scatter_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
+                                               ctypes.POINTER(_P), _P]),
+    "fsdp_allgather_copy_in_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
+                                             ctypes.POINTER(_P), _P]),
+    "fsdp_allgather_copy_out_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
+                                              ctypes.POINTER(_P), _P]),
     "fsdp_pack_reduce_scatter_noalloc": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_sync_status": (_ST, [_LAYOUT, _P]),
     "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
@@ -232,6 +238,41 @@ def fsdp_allgather_copy_in(layout: Layout, local_shards, ag_input, stream=None) 
 def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None) -> None:
     _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), pointer_array(full_params),
                                         _stream(stream)), "fsdp_allgather_copy_out")
+
+
+def layout_array(layouts):
+    """A C array of layout handles; pass it in place of a list to skip
+    re-marshalling on every call."""
+    if isinstance(layouts, ctypes.Array):
+        return layouts
+    arr = (_LAYOUT * max(1, len(layouts)))()
+    for k, L in enumerate(layouts):
+        arr[k] = L.handle
+    return arr
+
+
+def fsdp_pack_reduce_scatter_batched(layouts, grads, bucket_bufs, stream=None) -> None:
+    """grads / bucket_bufs: the per-layout lists concatenated in layout order."""
+    arr = layout_array(layouts)
+    _check(_lib.fsdp_pack_reduce_scatter_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
+                                                 pointer_array(grads), pointer_array(bucket_bufs), _stream(stream)),
+           "fsdp_pack_reduce_scatter_batched")
+
+
+def fsdp_allgather_copy_in_batched(layouts, local_shards, ag_inputs, stream=None) -> None:
+    """local_shards concatenated in layout order; one ag_input per layout."""
+    arr = layout_array(layouts)
+    _check(_lib.fsdp_allgather_copy_in_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
+                                               pointer_array(local_shards), pointer_array(ag_inputs), _stream(stream)),
+           "fsdp_allgather_copy_in_batched")
+
+
+def fsdp_allgather_copy_out_batched(layouts, ag_outputs, full_params, stream=None) -> None:
+    """One ag_output per layout; full_params concatenated in layout order."""
+    arr = layout_array(layouts)
+    _check(_lib.fsdp_allgather_copy_out_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
+                                                pointer_array(ag_outputs), pointer_array(full_params), _stream(stream)),
+           "fsdp_allgather_copy_out_batched")
 
 
 def fsdp_pack_reduce_scatter_noalloc(layout: Layout, grads, bucket_bufs, stream=None) -> None:

@@ -219,6 +219,34 @@ fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_out
                                       void *const *full_params, fsdp_stream_t stream);
 
 /*
+ * Batched calls: the work of several layouts (for instance every
+ * fully_shard group of a model, one per transformer block) in ONE kernel
+ * launch, with the same results as calling the single entry point once per
+ * layout, in order.  Small groups are bound by launch latency and the
+ * pipeline's ramp, not by HBM ("Training frameworks" note, "Group size and
+ * parameter retention": many tiny groups spend their time on latency); a
+ * batch pays those once.
+ *   layouts: host array of n_layouts layouts, all planned with a device
+ *            table on the current device (n_layouts <= 64).
+ *   Pointer arrays concatenate the per-layout arrays of the single calls, in
+ *   layout order: grads = layout 0's P_0 gradients, then layout 1's P_1, ...;
+ *   bucket_bufs likewise; local_shards and full_params likewise; ag_inputs
+ *   and ag_outputs hold one all-gather buffer per layout.  At most 3,840
+ *   pointers per batch (FSDP_EUNSUPPORTED above).
+ * Outputs of different layouts must not overlap.  A bounded-wait failure is
+ * recorded in the first layout's status word (fsdp_sync_status(layouts[0])).
+ */
+fsdp_status_t fsdp_pack_reduce_scatter_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                               const void *const *grads, void *const *bucket_bufs,
+                                               fsdp_stream_t stream);
+fsdp_status_t fsdp_allgather_copy_in_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                             const void *const *local_shards, void *const *ag_inputs,
+                                             fsdp_stream_t stream);
+fsdp_status_t fsdp_allgather_copy_out_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                              const void *const *ag_outputs, void *const *full_params,
+                                              fsdp_stream_t stream);
+
+/*
  * Reduce-scatter copy-in without any allocation.  The pages have no
  * counterpart: this is an extra entry point for callers that cannot allocate
  * device memory where they pack -- code that runs while another component

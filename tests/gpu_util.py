@@ -144,3 +144,53 @@ def fp_module():
     from fsdp2_gradient_packing_gb300 import fsdp_pack
     return fsdp_pack
 
+
+
+def assert_batched_parity(fp, runs):
+    """Push several GroupRuns through the batched entry points in single
+    launches and compare every group's outputs with the oracle."""
+    # Reduce-scatter copy-in: one launch for every group.
+    g_bufs, outs, rhos = [], [], []
+    for run in runs:
+        g_bufs += [DevBuf(g.nbytes, _offset(run.rng, ESZ[s.grad_dtype]), g) for s, g in zip(run.specs, run.grads)]
+        rho = ["f32" if d == oracle.F32 else "bf16" for d in run.pl.bucket_dtype]
+        rhos.append(rho)
+        outs.append([DevBuf(run.W * S * ESZ[r], _offset(run.rng, ESZ[r])) for r, S in zip(rho, run.pl.bucket_S)])
+    fp.fsdp_pack_reduce_scatter_batched([run.L for run in runs], [b.ptr for b in g_bufs],
+                                        [b.ptr for o in outs for b in o])
+    fp.fsdp_sync_status(runs[0].L)
+    for n, (run, out, rho) in enumerate(zip(runs, outs, rhos)):
+        for b, (buf, want, r) in enumerate(zip(out, run.pack_expected(), rho)):
+            got = buf.read(NP[r])
+            assert np.array_equal(got, want), f"batched pack, group {n}, bucket {b}: {first_mismatch(got, want)}"
+            assert buf.guards_ok()
+    assert all(b.guards_ok() for b in g_bufs)
+    # All-gather copy-in, rank by rank (layouts with fewer ranks drop out),
+    # then copy-out of every group in one launch.
+    gathered = [DevBuf(run.W * run.pl.S_ag, 0) for run in runs]
+    keep = []
+    for r in range(max(run.W for run in runs)):
+        sel = [k for k, run in enumerate(runs) if run.W > r]
+        shards = []
+        for k in sel:
+            run = runs[k]
+            bufs = [DevBuf(x.nbytes, _offset(run.rng, ESZ[s.shard_dtype]), x) for s, x in zip(run.specs, run.shards[r])]
+            keep += bufs
+            shards += [b.ptr for b in bufs]
+        fp.fsdp_allgather_copy_in_batched([runs[k].L for k in sel], shards,
+                                          [gathered[k].ptr + r * runs[k].pl.S_ag for k in sel])
+    full = [[DevBuf(s.numel * ESZ[s.param_dtype], _offset(run.rng, ESZ[s.param_dtype])) for s in run.specs]
+            for run in runs]
+    fp.fsdp_allgather_copy_out_batched([run.L for run in runs], [g.ptr for g in gathered],
+                                       [b.ptr for f in full for b in f])
+    fp.fsdp_sync_status(runs[0].L)
+    for n, run in enumerate(runs):
+        want_rows, want_full = run.gather_expected()
+        rows = gathered[n].read()
+        assert np.array_equal(rows, want_rows), f"batched copy-in, group {n}: {first_mismatch(rows, want_rows)}"
+        for p, (buf, s, want) in enumerate(zip(full[n], run.specs, want_full)):
+            got = buf.read(NP[s.param_dtype])
+            assert np.array_equal(got, want), f"batched copy-out, group {n} param {p}: {first_mismatch(got, want)}"
+            assert buf.guards_ok()
+        assert gathered[n].guards_ok()
+    assert all(b.guards_ok() for b in keep)

@@ -134,6 +134,24 @@ def test_entry_points_reject_host_only_layout_without_launching(fp):
             fp.fsdp_allgather_copy_out(L, 0x2000, [0x1000], stream=0)
 
 
+def test_batched_calls_check_their_arguments_without_launching(fp):
+    specs = wl.tiny_two_blocks(grouping="model").groups[0]
+    layouts = [fp.fsdp_plan_layout_host(specs, 4) for _ in range(65)]
+    try:
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_pack_reduce_scatter_batched(layouts, [0x1000] * (4 * 65), [0x2000] * 65, stream=0)
+        assert e.value.status == fp.FSDP_EUNSUPPORTED          # more than 64 layouts
+        for call, args in ((fp.fsdp_pack_reduce_scatter_batched, ([0x1000] * 8, [0x2000] * 2)),
+                           (fp.fsdp_allgather_copy_in_batched, ([0x1000] * 8, [0x2000] * 2)),
+                           (fp.fsdp_allgather_copy_out_batched, ([0x2000] * 2, [0x1000] * 8))):
+            with pytest.raises(fp.FsdpError) as e:
+                call(layouts[:2], *args, stream=0)
+            assert e.value.status == fp.FSDP_EINVAL             # host-only layouts
+    finally:
+        for L in layouts:
+            L.close()
+
+
 def test_query_index_out_of_range(fp):
     with fp.fsdp_plan_layout_host(wl.tiny_two_blocks().groups[0], 4) as L:
         for fn in (fp.fsdp_layout_param, fp.fsdp_layout_bucket, fp.fsdp_layout_group):

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from fsdp2_gradient_packing_gb300 import workloads as wl
-from gpu_util import DevBuf, ESZ, NP, GroupRun, assert_group_parity, first_mismatch
+from gpu_util import DevBuf, ESZ, NP, GroupRun, assert_batched_parity, assert_group_parity, first_mismatch
 
 pytestmark = pytest.mark.gpu
 
@@ -124,6 +124,44 @@ def test_many_parameters_use_the_larger_parameter_blocks(fp):
                       for i in range(n))
         work = wl.Workload(f"many{n}", 4, (specs,), std=1.0, seed=77)
         assert_group_parity(fp, specs, 4, work, 0, misalign_seed=n)
+
+
+def test_batched_transformer500_all_layers_in_one_launch(fp):
+    work = wl.transformer_500(W=8)
+    runs = [GroupRun(fp, specs, work.W, work, g) for g, specs in enumerate(work.groups)]
+    try:
+        assert_batched_parity(fp, runs)
+    finally:
+        for run in runs:
+            run.close()
+
+
+@pytest.mark.parametrize("batch", range(8))
+def test_batched_random_layouts_mixed_world_sizes(fp, batch):
+    rnd = np.random.default_rng(900 + batch)
+    n = int(rnd.integers(2, 9))
+    runs = []
+    try:
+        for k in range(n):
+            work = wl.random_layout(3000 + 16 * batch + k, max_params=6, max_numel=20000)
+            runs.append(GroupRun(fp, work.groups[0], work.W, work, 0, misalign_seed=batch * 16 + k, specials=0.02))
+        assert_batched_parity(fp, runs)
+    finally:
+        for run in runs:
+            run.close()
+
+
+def test_batched_with_empty_layouts(fp):
+    works = [wl.Workload("e0", 4, ((),), seed=1),
+             wl.tiny_two_blocks(W=4, grouping="model"),
+             wl.Workload("z", 2, ((wl.ParamSpec("z", (0,)), wl.ParamSpec("x", (7,), "bf16")),), seed=2)]
+    runs = [GroupRun(fp, w.groups[0], w.W, w, 0) for w in works]
+    try:
+        assert_batched_parity(fp, runs)
+        fp.fsdp_pack_reduce_scatter_batched([], [], [])
+    finally:
+        for run in runs:
+            run.close()
 
 
 def test_empty_layout_and_empty_parameters(fp):
