@@ -23,6 +23,10 @@ Sources (web pages, cited by title and section):
   dtype, reduce_dtype the gradient-reduction dtype, model.dtype the storage
   dtype of the resident shard.
 
+Operations: the reduce-scatter copy-in (pack), the all-gather copy-in and
+copy-out, and the reduce-scatter copy-out (reduced bucket rows to sharded
+gradients; [Unit] collective-count section).
+
 Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 values the pages print, closed forms, invariants, brute force on tiny inputs
 and an exact-rational rounding reference.  PARITY UNPINNED beyond element
@@ -77,7 +81,8 @@ def _bind(lib):
     lib.oracle_pack_samples.argtypes = [I32, P, P, P, P, P, I32, I32, I64, P, P, I64, P]
     lib.oracle_allgather_copy_in.argtypes = [I32, P, P, P, P, P, I32, P, I64, P, P]
     lib.oracle_allgather_copy_out.argtypes = [I32, I32, P, P, P, P, P, P, I64, P, P]
-    for name in ("oracle_pack_reduce_scatter", "oracle_pack_samples",
+    lib.oracle_reduce_scatter_copy_out.argtypes = [I32, P, P, P, P, P, P, P]
+    for name in ("oracle_pack_reduce_scatter", "oracle_pack_samples", "oracle_reduce_scatter_copy_out",
                  "oracle_allgather_copy_in", "oracle_allgather_copy_out",
                  "oracle_f32_to_bf16_array", "oracle_bf16_to_f32_array"):
         getattr(lib, name).restype = None
@@ -283,6 +288,20 @@ def params_from_specs(specs):
     """Oracle parameter descriptors from workload specs (dtype strings)."""
     return [Param(s.numel, _CODE[s.grad_dtype], _CODE[s.reduce_dtype],
                   _CODE[s.shard_dtype], _CODE[s.param_dtype]) for s in specs]
+
+
+def reduce_scatter_copy_out(pl: Plan, rows, out=None):
+    """This rank's reduced bucket rows (S_b elements each) -> per-parameter
+    sharded gradients (c_p elements of the shard dtype)."""
+    rows = [np.ascontiguousarray(r).reshape(-1) for r in rows]
+    for b, (dt, S) in enumerate(zip(pl.bucket_dtype, pl.bucket_S)):
+        _check(rows[b], dt, S, "reduced row")
+    if out is None:
+        out = [np.empty(c, DTYPE_NP[p.shard_dtype]) for p, c in zip(pl.params, pl.chunk)]
+    keep = [_i64(pl.chunk), _i32(pl.bucket_of), _i64(pl.bucket_off), _i32(pl.bucket_dtype),
+            _i32([p.shard_dtype for p in pl.params])]
+    _load().oracle_reduce_scatter_copy_out(len(pl.params), *(a.ctypes.data for a in keep), _ptrs(rows), _ptrs(out))
+    return out
 
 
 # ---------------------------------------------------------------------------

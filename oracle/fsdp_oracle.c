@@ -285,3 +285,24 @@ void oracle_allgather_copy_out(int32_t W, int32_t n_params, const int64_t *numel
       oracle_allgather_copy_out_segment(r, numel[p], chunk[p], param_dtype[p], group_elem_off[p],
                                         group_byte_off[group_of[p]], S_ag, ag_out, params[p]);
 }
+
+/* ---------------------------------------------------------------------------
+ * Reduce-scatter copy-out ([Unit] collective-count section: the reduce-scatter
+ * leaves every rank only the slice of the gradient that matches the
+ * parameters it owns; [NeMo] table: the resident sharded parameter, and so
+ * its gradient, is in the storage dtype).  Given this rank's reduced row of
+ * every bucket (S_b elements of rho_b), for every parameter p of bucket b and
+ * i < c_p:
+ *   sharded_grad_p[i] = cast_{rho_b -> sigma_p}(row_b[o_p + i])
+ * The c_p slots include the padding slots of the last ranks.
+ * ------------------------------------------------------------------------ */
+void oracle_reduce_scatter_copy_out(int32_t n_params, const int64_t *chunk, const int32_t *bucket_of,
+                                    const int64_t *bucket_off, const int32_t *bucket_dtype,
+                                    const int32_t *shard_dtype, const void *const *rows,
+                                    void *const *sharded) {
+  for (int32_t p = 0; p < n_params; ++p) {
+    int32_t b = bucket_of[p];
+    for (int64_t i = 0; i < chunk[p]; ++i)
+      cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);
+  }
+}

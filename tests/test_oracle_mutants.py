@@ -52,6 +52,12 @@ MUTANTS = {
     "copy-out: row stride taken as the chunk":
         ("const uint8_t *from = ag_out + (int64_t)r * S_ag + group_byte_off",
          "const uint8_t *from = ag_out + (int64_t)r * chunk * sz + group_byte_off"),
+    "rs copy-out: bucket offset dropped":
+        ("cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);",
+         "cast_element(rows[b], bucket_dtype[b], i, sharded[p], shard_dtype[p], i);"),
+    "rs copy-out: cast to the reduce dtype":
+        ("cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);",
+         "cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], bucket_dtype[b], i);"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and callable(getattr(pins, n))]

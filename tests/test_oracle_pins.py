@@ -476,3 +476,73 @@ def test_segment_entry_points_compose_to_the_whole_operations():
         for r in range(W):
             oracle.allgather_copy_out_segment(pl, gathered, full, p, r)
     assert all(np.array_equal(a, b) for a, b in zip(full, oracle.allgather_copy_out(pl, gathered)))
+
+
+# ---------------------------------------------------------------------------
+# Reduce-scatter copy-out: reduced bucket rows -> sharded gradients.
+# ---------------------------------------------------------------------------
+def brute_rs_copy_out(params, W, rows):
+    """Split each bucket row at the cumulative chunk sizes of its parameters
+    and cast each piece to the parameter's shard dtype."""
+    out = [None] * len(params)
+    for b, rd in enumerate(first_appearance([p.reduce_dtype for p in params])):
+        members = [k for k, p in enumerate(params) if p.reduce_dtype == rd]
+        sizes = [-(-params[k].numel // W) for k in members]
+        pieces = np.split(rows[b], np.cumsum(sizes)[:-1]) if members else []
+        for k, piece in zip(members, pieces):
+            out[k] = torch_cast(piece, rd, params[k].shard_dtype)
+    return out
+
+
+def test_rs_copy_out_gives_the_printed_grad_shards():
+    # [Unit], FlatParameter section: with one contributing rank the reduced
+    # row is rank 0's packed row, and its sharded gradient is the printed one.
+    g = sections("linear4x4_w2.txt")
+    grad = np.zeros((4, 4), np.float32)
+    grad[1] = np.float32(1.2830595970)
+    pl = plan([Param(16)], 2)
+    buf, = oracle.pack_reduce_scatter(pl, [grad.view(np.uint32).reshape(-1)])
+    shard0, = oracle.reduce_scatter_copy_out(pl, [buf[:8]])
+    shard1, = oracle.reduce_scatter_copy_out(pl, [buf[8:]])
+    assert np.array_equal(shard0, f32_bits(g["rank0_grad_shard"]))
+    assert np.array_equal(shard1, f32_bits(g["rank1_grad_shard"]))
+
+
+def test_rs_copy_out_brute_force_exhaustive_small():
+    dts = (F32, BF16)
+    k = 0
+    for W in range(1, 5):
+        for n1, n2 in itertools.product(range(0, 12, 3), range(0, 12, 2)):
+            for g1, r1, s1, r2, s2 in itertools.product(dts, dts, dts, dts, dts):
+                params = [Param(n1, g1, r1, s1), Param(n2, F32, r2, s2)]
+                pl = plan(params, W)
+                rng = np.random.default_rng(k)
+                rows = [rand_bits(rng, S, dt) for dt, S in zip(pl.bucket_dtype, pl.bucket_S)]
+                got = oracle.reduce_scatter_copy_out(pl, rows)
+                want = brute_rs_copy_out(params, W, rows)
+                for a, b in zip(got, want):
+                    assert a.dtype == b.dtype and np.array_equal(a, b), (params, W)
+                k += 1
+
+
+def test_pack_then_rs_copy_out_returns_each_ranks_chunk():
+    # With one contributing rank, row r of the packed buffer is the reduced
+    # row, and the sharded gradient is chunk r of the gradient, padded, cast
+    # g -> rho -> sigma.
+    rnd = random.Random(29)
+    rng = np.random.default_rng(29)
+    dts = (F32, BF16)
+    for k in range(200):
+        W = rnd.choice([1, 2, 3, 4, 8])
+        params = [Param(rnd.randint(0, 60), rnd.choice(dts), rnd.choice(dts), rnd.choice(dts))
+                  for _ in range(rnd.randint(1, 4))]
+        pl = plan(params, W)
+        grads = [rand_bits(rng, p.numel, p.grad_dtype) for p in params]
+        bufs = oracle.pack_reduce_scatter(pl, grads)
+        for r in range(W):
+            rows = [buf[r * S:(r + 1) * S] for buf, S in zip(bufs, pl.bucket_S)]
+            shards = oracle.reduce_scatter_copy_out(pl, rows)
+            for p, c, g, got in zip(params, pl.chunk, grads, shards):
+                chunk = np.pad(g, (0, c * W - p.numel)).reshape(W, c)[r] if c else g[:0]
+                want = torch_cast(torch_cast(chunk, p.grad_dtype, p.reduce_dtype), p.reduce_dtype, p.shard_dtype)
+                assert np.array_equal(got, want)
