@@ -59,6 +59,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 ESZ = {"f32": 4, "bf16": 2}
 STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
+STEP_RS = " + reduce-scatter copy-out (row 0 of each bucket as this rank's reduced row)"
 WORKLOADS = {
     # name: (factory, description); the first is the benchmark's workload.
     "mixed50m": (lambda: wl.mixed_50m(W=8),
@@ -90,6 +91,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed50m",
                     help="layout to time (the benchmark's metric is quoted on mixed50m)")
+    ap.add_argument("--rs-copy-out", action="store_true",
+                    help="add the reduce-scatter copy-out (reduced rows to sharded gradients) to every step")
     ap.add_argument("--batched", action="store_true",
                     help="one launch per operation for all of the workload's groups (*_batched entry points)")
     return ap.parse_args(argv)
@@ -141,7 +144,8 @@ def op_bytes(specs, W, bucket_bytes, S_ag):
     pack = sum(s.numel * ESZ[s.grad_dtype] for s in specs) + sum(bucket_bytes)
     copy_in = sum(ci * ESZ[s.shard_dtype] for ci, s in zip(c, specs)) + S_ag
     copy_out = 2 * sum(s.numel * ESZ[s.param_dtype] for s in specs)
-    return {"pack": pack, "copy_in": copy_in, "copy_out": copy_out}
+    rs_copy_out = sum(ci * (ESZ[s.reduce_dtype] + ESZ[s.shard_dtype]) for ci, s in zip(c, specs))
+    return {"pack": pack, "copy_in": copy_in, "copy_out": copy_out, "rs_copy_out": rs_copy_out}
 
 
 def read_peaks():
@@ -374,6 +378,13 @@ class DeviceSet:
         foffs, ftot = flat_offsets(f_sizes)
         self.full = torch.empty(ftot, dtype=torch.uint8, device=dev)
         self.full_ptrs = fp.pointer_array([self.full.data_ptr() + o for o in foffs])
+        # Reduce-scatter copy-out: row 0 of each bucket stands for this
+        # rank's reduced row; the sharded gradients go to their own buffer.
+        self.row0_ptrs = fp.pointer_array([b.data_ptr() for b in self.buckets])
+        h_sizes = [ci * ESZ[s.shard_dtype] for ci, s in zip(c, specs)]
+        hoffs, htot = flat_offsets(h_sizes)
+        self.sharded = torch.empty(htot, dtype=torch.uint8, device=dev)
+        self.sharded_ptrs = fp.pointer_array([self.sharded.data_ptr() + o for o in hoffs])
         # The other ranks' rows: what the all-gather would deliver.
         for r in range(W):
             if r == rank_row:
@@ -384,7 +395,7 @@ class DeviceSet:
             torch.cuda.synchronize()
             del other
 
-    def step(self, fp, L, h, ev=None):
+    def step(self, fp, L, h, ev=None, rs=False):
         if ev is not None:
             ev[0].record()
         fp.fsdp_pack_reduce_scatter(L, self.grad_ptrs, self.bucket_ptrs, h)
@@ -396,6 +407,10 @@ class DeviceSet:
         fp.fsdp_allgather_copy_out(L, self.gathered.data_ptr(), self.full_ptrs, h)
         if ev is not None:
             ev[3].record()
+        if rs:
+            fp.fsdp_reduce_scatter_copy_out(L, self.row0_ptrs, self.sharded_ptrs, h)
+            if ev is not None:
+                ev[4].record()
 
 
 class Group:
@@ -424,9 +439,10 @@ class Batch:
             self.sets.append(dict(
                 grads=cat(s.grad_ptrs for s in ss), buckets=cat(s.bucket_ptrs for s in ss),
                 shards=cat(s.shard_ptrs for s in ss), rows=fp.pointer_array([s.row_ptr for s in ss]),
-                gathered=fp.pointer_array([s.gathered.data_ptr() for s in ss]), full=cat(s.full_ptrs for s in ss)))
+                gathered=fp.pointer_array([s.gathered.data_ptr() for s in ss]), full=cat(s.full_ptrs for s in ss),
+                row0=cat(s.row0_ptrs for s in ss), sharded=cat(s.sharded_ptrs for s in ss)))
 
-    def step(self, fp, h, k, ev=None):
+    def step(self, fp, h, k, ev=None, rs=False):
         a = self.sets[k]
         if ev is not None:
             ev[0].record()
@@ -439,15 +455,19 @@ class Batch:
         fp.fsdp_allgather_copy_out_batched(self.layouts, a["gathered"], a["full"], h)
         if ev is not None:
             ev[3].record()
+        if rs:
+            fp.fsdp_reduce_scatter_copy_out_batched(self.layouts, a["row0"], a["sharded"], h)
+            if ev is not None:
+                ev[4].record()
 
 
-def run_steps(fp, groups, h, first, count, evs=None, batch=None):
+def run_steps(fp, groups, h, first, count, evs=None, batch=None, rs=False):
     for i in range(first, first + count):
         if batch is not None:
-            batch.step(fp, h, i & 1, None if evs is None else evs[i - first][0])
+            batch.step(fp, h, i & 1, None if evs is None else evs[i - first][0], rs)
             continue
         for gi, grp in enumerate(groups):
-            grp.sets[i & 1].step(fp, grp.L, h, None if evs is None else evs[i - first][gi])
+            grp.sets[i & 1].step(fp, grp.L, h, None if evs is None else evs[i - first][gi], rs)
 
 
 def run_ours(args):
@@ -463,12 +483,14 @@ def run_ours(args):
     work = factory()
     inputs = [host_inputs(work, g) for g in range(len(work.groups))]
     groups = [Group(fp, torch, work, g, inputs[g]) for g in range(len(work.groups))]
-    nbytes = {k: sum(grp.nbytes[k] for grp in groups) for k in ("pack", "copy_in", "copy_out")}
+    OPS = ("pack", "copy_in", "copy_out") + (("rs_copy_out",) if args.rs_copy_out else ())
+    nbytes = {k: sum(grp.nbytes[k] for grp in groups) for k in OPS}
     step_bytes = sum(nbytes.values())
     h = torch.cuda.current_stream().cuda_stream
     batch = Batch(fp, groups) if args.batched else None
     n_launch = 1 if batch is not None else len(groups)
-    run_steps(fp, groups, h, 0, args.warmup, batch=batch)
+    rs = args.rs_copy_out
+    run_steps(fp, groups, h, 0, args.warmup, batch=batch, rs=rs)
     for grp in groups:
         fp.fsdp_sync_status(grp.L)
 
@@ -487,7 +509,7 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first sample before the load starts
     t_start.record()
-    run_steps(fp, groups, h, 0, K, batch=batch)
+    run_steps(fp, groups, h, 0, K, batch=batch, rs=rs)
     t_end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -498,16 +520,16 @@ def run_ours(args):
 
     # Pass 2: the same K steps with a CUDA event around every launch, for the
     # per-operation device times (events between launches serialise them).
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_launch)] for _ in range(K)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(n_launch)]
+           for _ in range(K)]
     torch.cuda.synchronize()
     barrier()
-    run_steps(fp, groups, h, 0, K, evs, batch=batch)
+    run_steps(fp, groups, h, 0, K, evs, batch=batch, rs=rs)
     torch.cuda.synchronize()
     barrier()
     for grp in groups:
         fp.fsdp_sync_status(grp.L)
-    per = {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs]
-           for j, k in enumerate(("pack", "copy_in", "copy_out"))}
+    per = {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs] for j, k in enumerate(OPS)}
 
     # End to end through the same API with host buffers: every step copies
     # its inputs from pinned host memory and reads its results back.
@@ -517,13 +539,15 @@ def run_ours(args):
         s0 = grp.sets[0]
         hb = {"grads": pin(s0.grads.numel()), "shards": pin(s0.shards.numel()),
               "others": pin(s0.gathered.numel() - s0.S_ag),
-              "buckets": [pin(b.numel()) for b in s0.buckets], "full": pin(s0.full.numel())}
+              "buckets": [pin(b.numel()) for b in s0.buckets], "full": pin(s0.full.numel()),
+              "sharded": pin(s0.sharded.numel()) if rs else None}
         hb["grads"].copy_(s0.grads.cpu())
         hb["shards"].copy_(s0.shards.cpu())
         hb["others"].copy_(s0.gathered[s0.S_ag:].cpu())
         host.append(hb)
     h2d = sum(hb["grads"].numel() + hb["shards"].numel() + hb["others"].numel() for hb in host)
-    d2h = sum(sum(b.numel() for b in hb["buckets"]) + hb["full"].numel() for hb in host)
+    d2h = sum(sum(b.numel() for b in hb["buckets"]) + hb["full"].numel()
+              + (hb["sharded"].numel() if rs else 0) for hb in host)
     E = max(3, args.e2e_steps)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -535,10 +559,12 @@ def run_ours(args):
             s0.grads.copy_(hb["grads"], non_blocking=True)
             s0.shards.copy_(hb["shards"], non_blocking=True)
             s0.gathered[s0.S_ag:].copy_(hb["others"], non_blocking=True)
-            s0.step(fp, grp.L, h)
+            s0.step(fp, grp.L, h, None, rs)
             for hbuf, dbuf in zip(hb["buckets"], s0.buckets):
                 hbuf.copy_(dbuf, non_blocking=True)
             hb["full"].copy_(s0.full, non_blocking=True)
+            if rs:
+                hb["sharded"].copy_(s0.sharded, non_blocking=True)
     e_end.record()
     torch.cuda.synchronize()
     barrier()
@@ -568,7 +594,7 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "bf16+f32",
             "data": "synthetic",
-            "config": {"workload": f"{description}; {STEP}", "world_size_layout": work.W,
+            "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else ""), "world_size_layout": work.W,
                        "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
                        "parallelism": f"replicas x{world} (no data-path collective)",
                        "l2": "inputs larger than L2: two rotating buffer sets of "
@@ -583,7 +609,7 @@ def run_ours(args):
                          "traffic": read_traffic() if args.workload == "mixed50m" else None},
             "e2e": {"value": world * step_bytes * E / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E},
-            "gpu_launches": 3 * n_launch * K,
+            "gpu_launches": len(OPS) * n_launch * K,
             "clocks": clocks,
         }
     for grp in groups:

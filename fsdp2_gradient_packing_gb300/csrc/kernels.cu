@@ -775,6 +775,27 @@ fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_out
   return launch(L, OP_COPY_OUT, ptrs, P + 1, reinterpret_cast<cudaStream_t>(stream));
 }
 
+fsdp_status_t fsdp_reduce_scatter_copy_out(const fsdp_layout_t *L, const void *const *reduced_rows,
+                                           void *const *sharded_grads, fsdp_stream_t stream) {
+  fsdp_status_t st = check_layout(L);
+  if (st != FSDP_OK) return st;
+  const int P = (int)L->desc.size(), B = (int)L->bucket.size();
+  if (B > 0 && !reduced_rows) return fail(FSDP_EINVAL, "reduced_rows is NULL");
+  if (P > 0 && !sharded_grads) return fail(FSDP_EINVAL, "sharded_grads is NULL");
+  for (int b = 0; b < B; ++b) {
+    const int64_t sz = dtype_bytes(L->bucket[b].dtype);
+    if ((st = check_ptr(reduced_rows[b], L->bucket[b].S * sz, sz, "reduced_rows", b)) != FSDP_OK) return st;
+  }
+  for (int p = 0; p < P; ++p) {
+    const int64_t sz = dtype_bytes(L->desc[p].shard_dtype);
+    if ((st = check_ptr(sharded_grads[p], L->param[p].chunk * sz, sz, "sharded_grads", p)) != FSDP_OK) return st;
+  }
+  const void *ptrs[kSlotsLarge];
+  for (int b = 0; b < B; ++b) ptrs[b] = reduced_rows[b];
+  for (int p = 0; p < P; ++p) ptrs[B + p] = sharded_grads[p];
+  return launch(L, OP_RS_COPY_OUT, ptrs, B + P, reinterpret_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------------------
 // Batched calls: several layouts' work in one launch.
 // ---------------------------------------------------------------------------
@@ -876,6 +897,41 @@ fsdp_status_t fsdp_allgather_copy_out_batched(const fsdp_layout_t *const *layout
     }
   }
   return batch_launch(layouts, n_layouts, OP_COPY_OUT, ptrs, (int)at, base, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_reduce_scatter_copy_out_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                                   const void *const *reduced_rows, void *const *sharded_grads,
+                                                   fsdp_stream_t stream) {
+  fsdp_status_t st = check_batch(layouts, n_layouts);
+  if (st != FSDP_OK) return st;
+  int64_t n_rows = 0, n_grads = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) {
+    n_rows += (int64_t)layouts[g]->bucket.size();
+    n_grads += (int64_t)layouts[g]->desc.size();
+  }
+  if (n_rows + n_grads > kBatchSlotsLarge) return fail(FSDP_EUNSUPPORTED, "more than 3840 pointers in one batch");
+  if (n_rows > 0 && !reduced_rows) return fail(FSDP_EINVAL, "reduced_rows is NULL");
+  if (n_grads > 0 && !sharded_grads) return fail(FSDP_EINVAL, "sharded_grads is NULL");
+  const void *ptrs[kBatchSlotsLarge];
+  int32_t base[kMaxBatch];
+  int64_t ri = 0, gi = 0, at = 0;
+  for (int32_t g = 0; g < n_layouts; ++g) {
+    const fsdp_layout *L = layouts[g];
+    base[g] = (int32_t)at;
+    for (size_t b = 0; b < L->bucket.size(); ++b, ++ri) {
+      const int64_t sz = dtype_bytes(L->bucket[b].dtype);
+      if ((st = check_ptr(reduced_rows[ri], L->bucket[b].S * sz, sz, "reduced_rows", ri)) != FSDP_OK) return st;
+      ptrs[at++] = reduced_rows[ri];
+    }
+    for (size_t p = 0; p < L->desc.size(); ++p, ++gi) {
+      const int64_t sz = dtype_bytes(L->desc[p].shard_dtype);
+      if ((st = check_ptr(sharded_grads[gi], L->param[p].chunk * sz, sz, "sharded_grads", gi)) != FSDP_OK)
+        return st;
+      ptrs[at++] = sharded_grads[gi];
+    }
+  }
+  return batch_launch(layouts, n_layouts, OP_RS_COPY_OUT, ptrs, (int)at, base,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream) {

@@ -48,7 +48,7 @@ static_assert(sizeof(WorkItem) == 32, "work item must stay 32 bytes");
 constexpr int64_t kStageBytes = 8 * 1024;
 constexpr int64_t kItemDstBytes = 16 * 1024;
 
-enum Op { OP_PACK = 0, OP_COPY_IN = 1, OP_COPY_OUT = 2, OP_COUNT = 3 };
+enum Op { OP_PACK = 0, OP_COPY_IN = 1, OP_COPY_OUT = 2, OP_RS_COPY_OUT = 3, OP_COUNT = 4 };
 
 struct OpTable {
   int64_t first = 0;   // index of the op's first item in the shared table
@@ -89,7 +89,7 @@ struct fsdp_layout {
   std::vector<fsdp::BucketPlan> bucket;
   std::vector<fsdp::GroupPlan> group;
   int64_t S_ag = 0;
-  std::vector<fsdp::WorkItem> items;   // pack, copy-in, copy-out tables back to back
+  std::vector<fsdp::WorkItem> items;   // pack, copy-in, copy-out, rs copy-out tables back to back
   fsdp::OpTable op[fsdp::OP_COUNT];
   int64_t resident = 0;                // CTAs a launch keeps resident on the device
   fsdp::WorkItem *d_items = nullptr;   // device copy of `items`

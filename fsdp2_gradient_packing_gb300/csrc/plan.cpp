@@ -79,9 +79,12 @@ bool tables_consistent(const fsdp_layout &L) {
     } else if (op == OP_COPY_IN) {
       first_out = P;
       out_bytes.push_back(L.S_ag);
-    } else {
+    } else if (op == OP_COPY_OUT) {
       first_out = 1;
       for (int32_t p = 0; p < P; ++p) out_bytes.push_back(L.desc[p].numel * dtype_bytes(L.desc[p].param_dtype));
+    } else {
+      first_out = B;
+      for (int32_t p = 0; p < P; ++p) out_bytes.push_back(L.param[p].chunk * dtype_bytes(L.desc[p].shard_dtype));
     }
     std::vector<std::vector<Span>> spans(out_bytes.size());
     for (int64_t i = L.op[op].first; i < L.op[op].first + L.op[op].count; ++i) {
@@ -228,6 +231,16 @@ fsdp_status_t plan(const fsdp_param_desc_t *params, int32_t n, int32_t W, bool w
     }
     L->op[OP_COPY_OUT].count = (int64_t)items.size() - L->op[OP_COPY_OUT].first;
     L->op[OP_COPY_OUT].n_slots = P + 1;
+
+    // Reduce-scatter copy-out: slots [reduced rows 0..B) [sharded grads B..B+P).
+    L->op[OP_RS_COPY_OUT].first = (int64_t)items.size();
+    for (int32_t p = 0; p < P; ++p) {
+      const ParamPlan &pp = L->param[p];
+      emit_run(items, pp.bucket_off, 0, pp.chunk, pp.chunk, (uint16_t)pp.bucket, (uint16_t)(B + p),
+               kind_of(L->bucket[pp.bucket].dtype, params[p].shard_dtype), dtype_bytes(params[p].shard_dtype));
+    }
+    L->op[OP_RS_COPY_OUT].count = (int64_t)items.size() - L->op[OP_RS_COPY_OUT].first;
+    L->op[OP_RS_COPY_OUT].n_slots = B + P;
   } catch (const std::bad_alloc &) {
     delete L;
     return fail(FSDP_ENOMEM, "host allocation failed while planning");
@@ -288,6 +301,7 @@ fsdp_status_t fsdp_layout_query(const fsdp_layout_t *L, fsdp_layout_info_t *info
   info->pack_items = L->op[OP_PACK].count;
   info->copy_in_items = L->op[OP_COPY_IN].count;
   info->copy_out_items = L->op[OP_COPY_OUT].count;
+  info->rs_copy_out_items = L->op[OP_RS_COPY_OUT].count;
   clear_error();
   return FSDP_OK;
 }

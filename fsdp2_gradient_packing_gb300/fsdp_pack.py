@@ -43,7 +43,7 @@ class fsdp_layout_info_t(ctypes.Structure):
                 ("ag_bytes", ctypes.c_int64), ("total_numel", ctypes.c_int64),
                 ("device", ctypes.c_int32), ("has_device_table", ctypes.c_int32),
                 ("pack_items", ctypes.c_int64), ("copy_in_items", ctypes.c_int64),
-                ("copy_out_items", ctypes.c_int64)]
+                ("copy_out_items", ctypes.c_int64), ("rs_copy_out_items", ctypes.c_int64)]
 
 
 class fsdp_param_info_t(ctypes.Structure):
@@ -79,6 +79,9 @@ _SIGNATURES = {
     "fsdp_pack_reduce_scatter": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_allgather_copy_in": (_ST, [_LAYOUT, ctypes.POINTER(_P), _P, _P]),
     "fsdp_allgather_copy_out": (_ST, [_LAYOUT, _P, ctypes.POINTER(_P), _P]),
+    "fsdp_reduce_scatter_copy_out": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "fsdp_reduce_scatter_copy_out_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
+                                                   ctypes.POINTER(_P), _P]),
     "fsdp_pack_reduce_scatter_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
                                                ctypes.POINTER(_P), _P]),
     "fsdp_allgather_copy_in_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
@@ -240,6 +243,11 @@ def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None)
                                         _stream(stream)), "fsdp_allgather_copy_out")
 
 
+def fsdp_reduce_scatter_copy_out(layout: Layout, reduced_rows, sharded_grads, stream=None) -> None:
+    _check(_lib.fsdp_reduce_scatter_copy_out(layout.handle, pointer_array(reduced_rows), pointer_array(sharded_grads),
+                                             _stream(stream)), "fsdp_reduce_scatter_copy_out")
+
+
 def layout_array(layouts):
     """A C array of layout handles; pass it in place of a list to skip
     re-marshalling on every call."""
@@ -273,6 +281,14 @@ def fsdp_allgather_copy_out_batched(layouts, ag_outputs, full_params, stream=Non
     _check(_lib.fsdp_allgather_copy_out_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
                                                 pointer_array(ag_outputs), pointer_array(full_params), _stream(stream)),
            "fsdp_allgather_copy_out_batched")
+
+
+def fsdp_reduce_scatter_copy_out_batched(layouts, reduced_rows, sharded_grads, stream=None) -> None:
+    """reduced_rows / sharded_grads: the per-layout lists concatenated in layout order."""
+    arr = layout_array(layouts)
+    _check(_lib.fsdp_reduce_scatter_copy_out_batched(
+        arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts), pointer_array(reduced_rows),
+        pointer_array(sharded_grads), _stream(stream)), "fsdp_reduce_scatter_copy_out_batched")
 
 
 def fsdp_pack_reduce_scatter_noalloc(layout: Layout, grads, bucket_bufs, stream=None) -> None:

@@ -103,6 +103,7 @@ typedef struct {
   int64_t pack_items;       /* work items per call of each entry point */
   int64_t copy_in_items;
   int64_t copy_out_items;
+  int64_t rs_copy_out_items;
 } fsdp_layout_info_t;
 
 typedef struct {
@@ -219,6 +220,24 @@ fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_out
                                       void *const *full_params, fsdp_stream_t stream);
 
 /*
+ * Reduce-scatter copy-out: the step right after the reduce-scatter ([Unit],
+ * collective-count section: the reduce-scatter leaves each rank only the
+ * gradient slice of the parameters it owns; [NeMo] table: the resident
+ * sharded parameter, and so its gradient, is in the storage dtype).  Given
+ * this rank's reduced row of every bucket, for every parameter p of bucket b
+ * and i < c_p:
+ *   sharded_grads[p][i] = cast_{rho_b -> sigma_p}(reduced_rows[b][o_p + i])
+ * The c_p slots include the padding slots of the last ranks (they hold the
+ * reduction of the zero padding).  Casts as for fsdp_pack_reduce_scatter.
+ *   reduced_rows:  host array of n_buckets device pointers; row b holds S_b
+ *                  elements of rho_b (the reduce-scatter output of bucket b).
+ *   sharded_grads: host array of P device pointers; gradient p receives c_p
+ *                  elements of sigma_p.
+ */
+fsdp_status_t fsdp_reduce_scatter_copy_out(const fsdp_layout_t *L, const void *const *reduced_rows,
+                                           void *const *sharded_grads, fsdp_stream_t stream);
+
+/*
  * Batched calls: the work of several layouts (for instance every
  * fully_shard group of a model, one per transformer block) in ONE kernel
  * launch, with the same results as calling the single entry point once per
@@ -230,8 +249,8 @@ fsdp_status_t fsdp_allgather_copy_out(const fsdp_layout_t *L, const void *ag_out
  *            table on the current device (n_layouts <= 64).
  *   Pointer arrays concatenate the per-layout arrays of the single calls, in
  *   layout order: grads = layout 0's P_0 gradients, then layout 1's P_1, ...;
- *   bucket_bufs likewise; local_shards and full_params likewise; ag_inputs
- *   and ag_outputs hold one all-gather buffer per layout.  At most 3,840
+ *   bucket_bufs, reduced_rows, local_shards, full_params and sharded_grads
+ *   likewise; ag_inputs and ag_outputs hold one all-gather buffer per layout.  At most 3,840
  *   pointers per batch (FSDP_EUNSUPPORTED above).
  * Outputs of different layouts must not overlap.  A bounded-wait failure is
  * recorded in the first layout's status word (fsdp_sync_status(layouts[0])).
@@ -245,6 +264,9 @@ fsdp_status_t fsdp_allgather_copy_in_batched(const fsdp_layout_t *const *layouts
 fsdp_status_t fsdp_allgather_copy_out_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
                                               const void *const *ag_outputs, void *const *full_params,
                                               fsdp_stream_t stream);
+fsdp_status_t fsdp_reduce_scatter_copy_out_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
+                                                   const void *const *reduced_rows, void *const *sharded_grads,
+                                                   fsdp_stream_t stream);
 
 /*
  * Reduce-scatter copy-in without any allocation.  The pages have no

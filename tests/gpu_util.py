@@ -60,10 +60,19 @@ class GroupRun:
     def __init__(self, fp, specs, W: int, work: wl.Workload, group: int, misalign_seed=None,
                  specials: float = 0.0):
         self.fp, self.specs, self.W = fp, list(specs), W
+        self.work, self.group = work, group
         self.pl = oracle.plan(oracle.params_from_specs(specs), W)
         self.L = fp.fsdp_plan_layout(specs, W)
         self.rng = np.random.default_rng(misalign_seed) if misalign_seed is not None else None
         self.grads = [wl.grad_values(work, group, i, specials=specials) for i in range(len(specs))]
+        # This rank's reduced bucket rows (the reduce-scatter output).
+        self.rows = []
+        for b, (dt, S) in enumerate(zip(self.pl.bucket_dtype, self.pl.bucket_S)):
+            name = "f32" if dt == oracle.F32 else "bf16"
+            bits = wl.normal_bits(S, name, work.std, work.seed, group, 4, b)
+            if specials:
+                wl.inject_specials(bits, name, specials, work.seed, group, 4, b)
+            self.rows.append(bits)
         self.shards = []
         for r in range(W):
             row = []
@@ -89,6 +98,20 @@ class GroupRun:
 
     def pack_expected(self):
         return oracle.pack_reduce_scatter(self.pl, self.grads)
+
+    # -- reduce-scatter copy-out -------------------------------------------
+    def rs_copy_out(self):
+        fp, pl = self.fp, self.pl
+        rho = ["f32" if d == oracle.F32 else "bf16" for d in pl.bucket_dtype]
+        rows = [DevBuf(x.nbytes, _offset(self.rng, ESZ[r]), x) for x, r in zip(self.rows, rho)]
+        outs = [DevBuf(c * ESZ[s.shard_dtype], _offset(self.rng, ESZ[s.shard_dtype])) for s, c in zip(self.specs, pl.chunk)]
+        fp.fsdp_reduce_scatter_copy_out(self.L, [b.ptr for b in rows], [b.ptr for b in outs])
+        fp.fsdp_sync_status(self.L)
+        got = [b.read(NP[s.shard_dtype]) for b, s in zip(outs, self.specs)]
+        return got, all(b.guards_ok() for b in rows + outs)
+
+    def rs_copy_out_expected(self):
+        return oracle.reduce_scatter_copy_out(self.pl, self.rows)
 
     # -- all-gather copy-in (every rank into its row) and copy-out ------------
     def gather(self):
@@ -130,6 +153,10 @@ def assert_group_parity(fp, specs, W, work, group, misalign_seed=None, specials=
         assert ok, "guard bytes around pack buffers changed"
         for b, (x, y) in enumerate(zip(got, run.pack_expected())):
             assert np.array_equal(x, y), f"pack bucket {b}: {first_mismatch(x, y)}"
+        got, ok = run.rs_copy_out()
+        assert ok, "guard bytes around reduce-scatter copy-out buffers changed"
+        for p, (x, y) in enumerate(zip(got, run.rs_copy_out_expected())):
+            assert np.array_equal(x, y), f"rs copy-out param {p}: {first_mismatch(x, y)}"
         rows, full, ok = run.gather()
         assert ok, "guard bytes around all-gather buffers changed"
         want_rows, want_full = run.gather_expected()
@@ -165,6 +192,22 @@ def assert_batched_parity(fp, runs):
             assert np.array_equal(got, want), f"batched pack, group {n}, bucket {b}: {first_mismatch(got, want)}"
             assert buf.guards_ok()
     assert all(b.guards_ok() for b in g_bufs)
+    # Reduce-scatter copy-out of every group in one launch.
+    rows, sharded = [], []
+    for run in runs:
+        rho = ["f32" if d == oracle.F32 else "bf16" for d in run.pl.bucket_dtype]
+        rows += [DevBuf(x.nbytes, _offset(run.rng, ESZ[r]), x) for x, r in zip(run.rows, rho)]
+        sharded.append([DevBuf(c * ESZ[s.shard_dtype], _offset(run.rng, ESZ[s.shard_dtype]))
+                        for s, c in zip(run.specs, run.pl.chunk)])
+    fp.fsdp_reduce_scatter_copy_out_batched([run.L for run in runs], [b.ptr for b in rows],
+                                            [b.ptr for sh in sharded for b in sh])
+    fp.fsdp_sync_status(runs[0].L)
+    for n, (run, sh) in enumerate(zip(runs, sharded)):
+        for p, (buf, s, want) in enumerate(zip(sh, run.specs, run.rs_copy_out_expected())):
+            got = buf.read(NP[s.shard_dtype])
+            assert np.array_equal(got, want), f"batched rs copy-out, group {n} param {p}: {first_mismatch(got, want)}"
+            assert buf.guards_ok()
+    assert all(b.guards_ok() for b in rows)
     # All-gather copy-in, rank by rank (layouts with fewer ranks drop out),
     # then copy-out of every group in one launch.
     gathered = [DevBuf(run.W * run.pl.S_ag, 0) for run in runs]

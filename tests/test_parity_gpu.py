@@ -105,6 +105,11 @@ def test_kda_block_full_size(fp, W, reduce):
             want = oracle.pack_samples(run.pl, run.grads, b, idx)
             assert np.array_equal(got[b][idx], want), f"bucket {b}: {first_mismatch(got[b][idx], want)}"
         del got
+        got, ok = run.rs_copy_out()
+        assert ok
+        for x, y in zip(got, run.rs_copy_out_expected()):
+            assert np.array_equal(x, y), first_mismatch(x, y)
+        del got
         if reduce == "f32":
             rows, full, ok = run.gather()
             assert ok
