@@ -109,8 +109,8 @@ bool tables_consistent(const fsdp_layout &L) {
   return true;
 }
 
-fsdp_status_t plan(const fsdp_param_desc_t *params, int32_t n, int32_t W, bool with_device,
-                   fsdp_layout_t **out) {
+fsdp_status_t plan(const fsdp_param_desc_t *params, const int64_t *row_elems, int32_t n, int32_t W,
+                   bool with_device, fsdp_layout_t **out) {
   if (!out) return fail(FSDP_EINVAL, "out is NULL");
   *out = nullptr;
   if (n < 0) return fail(FSDP_EINVAL, "n_params < 0");
@@ -127,6 +127,8 @@ fsdp_status_t plan(const fsdp_param_desc_t *params, int32_t n, int32_t W, bool w
     // split into items, so only the byte offsets below need 64 bits.
     if (d.numel > (int64_t(1) << 46))
       return fail(FSDP_EUNSUPPORTED, "params[" + std::to_string(p) + "].numel above 2^46");
+    if (row_elems && (row_elems[p] < 0 || (row_elems[p] > 0 && d.numel % row_elems[p] != 0)))
+      return fail(FSDP_EINVAL, "row_elems[" + std::to_string(p) + "] is negative or does not divide numel");
   }
 
   fsdp_layout *L = new (std::nothrow) fsdp_layout();
@@ -139,7 +141,12 @@ fsdp_status_t plan(const fsdp_param_desc_t *params, int32_t n, int32_t W, bool w
     for (int32_t p = 0; p < n; ++p) {
       const fsdp_param_desc_t &d = params[p];
       ParamPlan &pp = L->param[p];
-      pp.chunk = ceil_div(d.numel, W);
+      // Flattened: ceil(n_p / W) elements.  Row chunks: ceil(d0 / W) rows of
+      // row_elems elements, d0 = n_p / row_elems.
+      if (row_elems && row_elems[p] > 0)
+        pp.chunk = ceil_div(d.numel / row_elems[p], W) * row_elems[p];
+      else
+        pp.chunk = ceil_div(d.numel, W);
       int32_t b = -1;
       for (size_t k = 0; k < L->bucket.size(); ++k)
         if (L->bucket[k].dtype == d.reduce_dtype) b = (int32_t)k;
@@ -279,12 +286,18 @@ extern "C" {
 
 fsdp_status_t fsdp_plan_layout(const fsdp_param_desc_t *params, int32_t n_params, int32_t world_size,
                                fsdp_layout_t **out) {
-  return plan(params, n_params, world_size, true, out);
+  return plan(params, nullptr, n_params, world_size, true, out);
 }
 
 fsdp_status_t fsdp_plan_layout_host(const fsdp_param_desc_t *params, int32_t n_params,
                                     int32_t world_size, fsdp_layout_t **out) {
-  return plan(params, n_params, world_size, false, out);
+  return plan(params, nullptr, n_params, world_size, false, out);
+}
+
+fsdp_status_t fsdp_plan_layout_ex(const fsdp_param_desc_t *params, const int64_t *row_elems, int32_t n_params,
+                                  int32_t world_size, uint32_t flags, fsdp_layout_t **out) {
+  if (flags & ~(uint32_t)FSDP_PLAN_HOST_ONLY) return fail(FSDP_EINVAL, "unknown plan flags");
+  return plan(params, row_elems, n_params, world_size, (flags & FSDP_PLAN_HOST_ONLY) == 0, out);
 }
 
 fsdp_status_t fsdp_layout_query(const fsdp_layout_t *L, fsdp_layout_info_t *info) {

@@ -29,6 +29,7 @@ DTYPE_BYTES = {FSDP_DTYPE_F32: 4, FSDP_DTYPE_BF16: 2}
 
 FSDP_OK, FSDP_EINVAL, FSDP_ENOMEM, FSDP_ECUDA, FSDP_EUNSUPPORTED, FSDP_ETIMEOUT = range(6)
 FSDP_MAX_PARAMS = 4000
+FSDP_PLAN_HOST_ONLY = 1
 
 
 class fsdp_param_desc_t(ctypes.Structure):
@@ -72,6 +73,8 @@ _SIGNATURES = {
                                ctypes.POINTER(_LAYOUT)]),
     "fsdp_plan_layout_host": (_ST, [ctypes.POINTER(fsdp_param_desc_t), ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(_LAYOUT)]),
+    "fsdp_plan_layout_ex": (_ST, [ctypes.POINTER(fsdp_param_desc_t), ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_uint32, ctypes.POINTER(_LAYOUT)]),
     "fsdp_layout_query": (_ST, [_LAYOUT, ctypes.POINTER(fsdp_layout_info_t)]),
     "fsdp_layout_param": (_ST, [_LAYOUT, ctypes.c_int32, ctypes.POINTER(fsdp_param_info_t)]),
     "fsdp_layout_bucket": (_ST, [_LAYOUT, ctypes.c_int32, ctypes.POINTER(fsdp_bucket_info_t)]),
@@ -174,6 +177,29 @@ def fsdp_plan_layout_host(params, world_size: int) -> Layout:
     _check(_lib.fsdp_plan_layout_host(arr, len(params), world_size, ctypes.byref(out)),
            "fsdp_plan_layout_host")
     return Layout(out.value, len(params))
+
+
+def fsdp_plan_layout_ex(params, world_size: int, row_elems=None, flags: int = 0) -> Layout:
+    """row_elems: per-parameter elements per dim-0 row (0 = flattened), or None."""
+    arr = _descs(params)
+    rows = None
+    if row_elems is not None:
+        rows = (ctypes.c_int64 * max(1, len(row_elems)))(*row_elems)
+    out = _LAYOUT()
+    _check(_lib.fsdp_plan_layout_ex(arr, rows, len(params), world_size, flags, ctypes.byref(out)),
+           "fsdp_plan_layout_ex")
+    return Layout(out.value, len(params))
+
+
+def row_elems_of(specs):
+    """Elements per dim-0 row of each spec's shape (1 for 1-D parameters)."""
+    out = []
+    for s in specs:
+        r = 1
+        for d in s.shape[1:]:
+            r *= d
+        out.append(r)
+    return out
 
 
 def fsdp_layout_query(layout: Layout) -> fsdp_layout_info_t:

@@ -261,3 +261,18 @@ def random_layout(seed: int, max_params: int = 6, max_numel: int = 300,
         g.append(ParamSpec(f"p{i}", (numel,), rnd.choice(dts), rnd.choice(dts),
                            rnd.choice(dts), rnd.choice(dts)))
     return Workload(f"random{seed}", W, (tuple(g),), std=1.0, seed=5000 + seed)
+
+
+def random_layout_2d(seed: int, max_params: int = 5, max_rows: int = 300, max_row: int = 64,
+                     W_choices=(1, 2, 3, 5, 6, 7, 8, 16, 64)) -> Workload:
+    """A seeded random single-group layout of 1-D and 2-D parameters, for the
+    dim-0 row-chunk rule (world sizes that often do not divide d0)."""
+    rnd = random.Random(seed)
+    W = rnd.choice(W_choices)
+    dts = ("f32", "bf16")
+    g = []
+    for i in range(rnd.randint(1, max_params)):
+        d0 = 0 if rnd.random() < 0.08 else rnd.randint(1, max_rows)
+        shape = (d0,) if rnd.random() < 0.25 else (d0, rnd.randint(1, max_row))
+        g.append(ParamSpec(f"p{i}", shape, rnd.choice(dts), rnd.choice(dts), rnd.choice(dts), rnd.choice(dts)))
+    return Workload(f"random2d{seed}", W, (tuple(g),), std=1.0, seed=7000 + seed)

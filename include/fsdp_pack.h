@@ -160,6 +160,27 @@ fsdp_status_t fsdp_plan_layout(const fsdp_param_desc_t *params, int32_t n_params
 fsdp_status_t fsdp_plan_layout_host(const fsdp_param_desc_t *params, int32_t n_params,
                                     int32_t world_size, fsdp_layout_t **out);
 
+/*
+ * Planning with dim-0 row chunks (FSDP2's own sharding of a parameter: zero-
+ * padded along dim 0 to a multiple of W rows and split into W row chunks).
+ *   row_elems: host array of n_params values, or NULL.  row_elems[p] > 0 is
+ *              the number of elements in one dim-0 row of parameter p (the
+ *              product of its other dims; it must divide numel), and gives
+ *              c_p = ceil((numel / row_elems[p]) / W) * row_elems[p]: rank r
+ *              owns rows [r*ceil(d0/W), (r+1)*ceil(d0/W)).  row_elems[p] == 0
+ *              (or a NULL array) keeps the flattened rule c_p = ceil(n_p / W).
+ *              The two rules agree whenever W divides d0.
+ *   flags:     0, or FSDP_PLAN_HOST_ONLY to plan without any CUDA call (as
+ *              fsdp_plan_layout_host).
+ * Everything else -- buckets, groups, offsets, all entry points -- follows
+ * from c_p exactly as for fsdp_plan_layout.  Errors as for fsdp_plan_layout,
+ * plus FSDP_EINVAL for a negative row_elems, one that does not divide numel,
+ * or unknown flags.
+ */
+#define FSDP_PLAN_HOST_ONLY 1u
+fsdp_status_t fsdp_plan_layout_ex(const fsdp_param_desc_t *params, const int64_t *row_elems, int32_t n_params,
+                                  int32_t world_size, uint32_t flags, fsdp_layout_t **out);
+
 /* Host-only queries; no CUDA call, no synchronisation.  Index arguments out
  * of range give FSDP_EINVAL. */
 fsdp_status_t fsdp_layout_query(const fsdp_layout_t *L, fsdp_layout_info_t *info);

@@ -134,12 +134,17 @@ def _align16(x: int) -> int:
     return _ceil_div(x, 16) * 16
 
 
-def plan(params, W: int) -> Plan:
+def plan(params, W: int, row_elems=None) -> Plan:
     """Layout of one fully_shard group.
 
     c_p = ceil(n_p / W): the flattened parameter padded on the right to c_p*W
     elements and split into W equal contiguous slices ([Unit], FlatParameter
-    and padding sections).  Buckets: one per distinct reduce dtype, in order of
+    and padding sections).  With ``row_elems`` (elements per dim-0 row of
+    each parameter; 0 keeps the flattened rule for that parameter) a
+    parameter of d0 = n_p / row_elems rows is instead padded along dim 0 to a
+    multiple of W rows and split into W row chunks: c_p = ceil(d0 / W) *
+    row_elems, and rank r's chunk is rows [r*ceil(d0/W), (r+1)*ceil(d0/W)),
+    i.e. flat elements [r*c_p, (r+1)*c_p) again.  Buckets: one per distinct reduce dtype, in order of
     first appearance; inside a bucket parameters keep registration order
     ([News] paragraph 2).  All-gather groups: one per distinct (shard dtype,
     param dtype) pair, in order of first appearance ([News] paragraph 1); each
@@ -150,10 +155,16 @@ def plan(params, W: int) -> Plan:
     pl = Plan(W=W, params=list(params))
     bucket_index = {}
     group_index = {}
-    for p in pl.params:
+    for k, p in enumerate(pl.params):
         if p.numel < 0:
             raise ValueError("numel must be >= 0")
-        c = _ceil_div(p.numel, W)
+        rows_of = row_elems[k] if row_elems is not None else 0
+        if rows_of:
+            if p.numel % rows_of:
+                raise ValueError("numel must be a multiple of row_elems")
+            c = _ceil_div(p.numel // rows_of, W) * rows_of
+        else:
+            c = _ceil_div(p.numel, W)
         pl.chunk.append(c)
         if p.reduce_dtype not in bucket_index:
             bucket_index[p.reduce_dtype] = len(pl.bucket_dtype)

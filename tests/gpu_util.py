@@ -58,11 +58,12 @@ class GroupRun:
     """One group through the CUDA library and the oracle."""
 
     def __init__(self, fp, specs, W: int, work: wl.Workload, group: int, misalign_seed=None,
-                 specials: float = 0.0):
+                 specials: float = 0.0, rows: bool = False):
         self.fp, self.specs, self.W = fp, list(specs), W
         self.work, self.group = work, group
-        self.pl = oracle.plan(oracle.params_from_specs(specs), W)
-        self.L = fp.fsdp_plan_layout(specs, W)
+        row_elems = fp.row_elems_of(specs) if rows else None
+        self.pl = oracle.plan(oracle.params_from_specs(specs), W, row_elems=row_elems)
+        self.L = fp.fsdp_plan_layout_ex(specs, W, row_elems) if rows else fp.fsdp_plan_layout(specs, W)
         self.rng = np.random.default_rng(misalign_seed) if misalign_seed is not None else None
         self.grads = [wl.grad_values(work, group, i, specials=specials) for i in range(len(specs))]
         # This rank's reduced bucket rows (the reduce-scatter output).
@@ -146,8 +147,8 @@ def first_mismatch(a: np.ndarray, b: np.ndarray) -> str:
     return f"{bad.size} mismatches, first at {i}: got {a[i]:#x} want {b[i]:#x}"
 
 
-def assert_group_parity(fp, specs, W, work, group, misalign_seed=None, specials=0.0):
-    run = GroupRun(fp, specs, W, work, group, misalign_seed, specials)
+def assert_group_parity(fp, specs, W, work, group, misalign_seed=None, specials=0.0, rows=False):
+    run = GroupRun(fp, specs, W, work, group, misalign_seed, specials, rows)
     try:
         got, ok = run.pack()
         assert ok, "guard bytes around pack buffers changed"

@@ -44,9 +44,12 @@ def test_binding_has_a_function_per_entry_point(fp):
         assert callable(getattr(fp, n)), n
 
 
-def _compare_with_oracle(fp, specs, W):
-    pl = oracle.plan(oracle.params_from_specs(specs), W)
-    with fp.fsdp_plan_layout_host(specs, W) as L:
+def _compare_with_oracle(fp, specs, W, rows=False):
+    row_elems = fp.row_elems_of(specs) if rows else None
+    pl = oracle.plan(oracle.params_from_specs(specs), W, row_elems=row_elems)
+    plan = (lambda: fp.fsdp_plan_layout_ex(specs, W, row_elems, fp.FSDP_PLAN_HOST_ONLY)) if rows else \
+        (lambda: fp.fsdp_plan_layout_host(specs, W))
+    with plan() as L:
         info = fp.fsdp_layout_query(L)
         assert info.world_size == W and info.n_params == len(specs)
         assert info.n_buckets == len(pl.bucket_dtype) and info.n_groups == len(pl.group_pair)
@@ -86,6 +89,28 @@ def test_host_plan_matches_oracle_on_random_layouts(fp):
     for seed in range(400):
         work = wl.random_layout(seed)
         _compare_with_oracle(fp, work.groups[0], work.W)
+
+
+def test_row_mode_host_plan_matches_oracle(fp):
+    for seed in range(300):
+        work = wl.random_layout_2d(seed)
+        _compare_with_oracle(fp, work.groups[0], work.W, rows=True)
+    for make in (lambda: wl.transformer_500(W=7, layers=2), lambda: wl.kda_block(W=64, d=512, ffn=1536)):
+        work = make()
+        for g in work.groups:
+            _compare_with_oracle(fp, g, work.W, rows=True)
+
+
+def test_row_mode_rejects_bad_rows_and_flags(fp):
+    specs = [wl.ParamSpec("w", (6, 6))]
+    for rows, flags in (([-1], 1), ([7], 1), ([6], 1 | 2)):
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_plan_layout_ex(specs, 4, rows, flags)
+        assert e.value.status == fp.FSDP_EINVAL
+    with fp.fsdp_plan_layout_ex(specs, 4, [6], fp.FSDP_PLAN_HOST_ONLY) as L:
+        assert fp.fsdp_layout_param(L, 0).chunk == 12
+    with fp.fsdp_plan_layout_ex(specs, 4, [0], fp.FSDP_PLAN_HOST_ONLY) as L:
+        assert fp.fsdp_layout_param(L, 0).chunk == 9
 
 
 def test_empty_layout(fp):

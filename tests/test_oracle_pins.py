@@ -546,3 +546,63 @@ def test_pack_then_rs_copy_out_returns_each_ranks_chunk():
                 chunk = np.pad(g, (0, c * W - p.numel)).reshape(W, c)[r] if c else g[:0]
                 want = torch_cast(torch_cast(chunk, p.grad_dtype, p.reduce_dtype), p.reduce_dtype, p.shard_dtype)
                 assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# Row-chunk mode: pad along dim 0 to a multiple of W rows, split in W row chunks.
+# ---------------------------------------------------------------------------
+def brute_pack_rows(params, shapes, W, grads):
+    """Definition written with 2-D arrays: pad the (d0, row) view of each
+    gradient with zero rows to a multiple of W, split it into W row chunks,
+    and lay every parameter's chunk r side by side in row r."""
+    outs = []
+    for rd in first_appearance([p.reduce_dtype for p in params]):
+        blocks = []
+        for p, (d0, row), g in zip(params, shapes, grads):
+            if p.reduce_dtype != rd:
+                continue
+            v = torch_cast(g, p.grad_dtype, rd).reshape(d0, row)
+            rows_per_rank = -(-d0 // W)
+            v = np.pad(v, ((0, rows_per_rank * W - d0), (0, 0)))
+            blocks.append(v.reshape(W, rows_per_rank * row))
+        outs.append(np.hstack(blocks).reshape(-1))
+    return outs
+
+
+def test_row_mode_pack_matches_the_row_definition():
+    rnd = random.Random(31)
+    dts = (F32, BF16)
+    for k in range(400):
+        W = rnd.choice([1, 2, 3, 4, 5, 7, 8])
+        shapes = [(rnd.randint(0, 11), rnd.randint(1, 6)) for _ in range(rnd.randint(1, 4))]
+        params = [Param(d0 * row, rnd.choice(dts), rnd.choice(dts)) for d0, row in shapes]
+        pl = plan(params, W, row_elems=[row for _, row in shapes])
+        rng = np.random.default_rng(k)
+        grads = [rand_bits(rng, p.numel, p.grad_dtype) for p in params]
+        got = oracle.pack_reduce_scatter(pl, grads)
+        want = brute_pack_rows(params, shapes, W, grads)
+        for a, b in zip(got, want):
+            assert np.array_equal(a, b), (shapes, W)
+
+
+def test_row_mode_agrees_with_flattening_when_rows_divide():
+    rnd = random.Random(37)
+    for k in range(200):
+        W = rnd.choice([1, 2, 4, 8])
+        shapes = [(W * rnd.randint(0, 5), rnd.randint(1, 9)) for _ in range(rnd.randint(1, 4))]
+        params = [Param(d0 * row, BF16, F32, F32, BF16) for d0, row in shapes]
+        a = plan(params, W, row_elems=[row for _, row in shapes])
+        b = plan(params, W)
+        assert a.chunk == b.chunk and a.bucket_S == b.bucket_S and a.S_ag == b.S_ag
+
+
+def test_row_mode_linear_examples():
+    # Linear(4, 4) at W = 2: two rows per rank either way, so the printed
+    # shard of rank 0 (rows 0-1) is the same under both readings.
+    assert plan([Param(16)], 2, row_elems=[4]).chunk == plan([Param(16)], 2).chunk == [8]
+    # Linear(6, 6) at W = 4: ceil(6/4) = 2 rows = 12 elements per rank in row
+    # mode, against the flattened 9 that the wrap-policy printout shows.
+    assert plan([Param(36)], 4, row_elems=[6]).chunk == [12]
+    assert plan([Param(36)], 4).chunk == [9]
+    # Linear(3, 3) at W = 4: one row per rank in row mode, 4 rows = 12 slots.
+    assert plan([Param(9)], 4, row_elems=[3]).chunk == [3]

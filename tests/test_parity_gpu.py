@@ -131,6 +131,27 @@ def test_many_parameters_use_the_larger_parameter_blocks(fp):
         assert_group_parity(fp, specs, 4, work, 0, misalign_seed=n)
 
 
+@pytest.mark.parametrize("chunk", range(4))
+def test_row_chunk_mode_random_2d_layouts(fp, chunk):
+    """Dim-0 row chunks (FSDP2's own sharding) with world sizes that often do
+    not divide d0: all four operations against the oracle's row rule."""
+    for seed in range(chunk * 40, (chunk + 1) * 40):
+        work = wl.random_layout_2d(seed, max_rows=400, max_row=96)
+        assert_group_parity(fp, work.groups[0], work.W, work, 0, misalign_seed=seed, specials=0.03, rows=True)
+
+
+def test_row_chunk_mode_batched(fp):
+    runs = []
+    try:
+        for k in range(6):
+            work = wl.random_layout_2d(500 + k)
+            runs.append(GroupRun(fp, work.groups[0], work.W, work, 0, misalign_seed=k, specials=0.03, rows=True))
+        assert_batched_parity(fp, runs)
+    finally:
+        for run in runs:
+            run.close()
+
+
 def test_batched_transformer500_all_layers_in_one_launch(fp):
     work = wl.transformer_500(W=8)
     runs = [GroupRun(fp, specs, work.W, work, g) for g, specs in enumerate(work.groups)]
