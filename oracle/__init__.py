@@ -24,8 +24,10 @@ Sources (web pages, cited by title and section):
   dtype of the resident shard.
 
 Operations: the reduce-scatter copy-in (pack), the all-gather copy-in and
-copy-out, and the reduce-scatter copy-out (reduced bucket rows to sharded
-gradients; [Unit] collective-count section).
+copy-out, the reduce-scatter copy-out (reduced bucket rows to sharded
+gradients; [Unit] collective-count section), and an emulated reduce-scatter
+(elementwise sum of every rank's packed buffer in rank order, partial sums
+rounded to the bucket dtype) for end-to-end tests without a network.
 
 Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 values the pages print, closed forms, invariants, brute force on tiny inputs
@@ -82,6 +84,8 @@ def _bind(lib):
     lib.oracle_allgather_copy_in.argtypes = [I32, P, P, P, P, P, I32, P, I64, P, P]
     lib.oracle_allgather_copy_out.argtypes = [I32, I32, P, P, P, P, P, P, I64, P, P]
     lib.oracle_reduce_scatter_copy_out.argtypes = [I32, P, P, P, P, P, P, P]
+    lib.oracle_emulated_reduce_scatter.argtypes = [I64, I32, I32, P, P]
+    lib.oracle_emulated_reduce_scatter.restype = None
     for name in ("oracle_pack_reduce_scatter", "oracle_pack_samples", "oracle_reduce_scatter_copy_out",
                  "oracle_allgather_copy_in", "oracle_allgather_copy_out",
                  "oracle_f32_to_bf16_array", "oracle_bf16_to_f32_array"):
@@ -312,6 +316,22 @@ def reduce_scatter_copy_out(pl: Plan, rows, out=None):
     keep = [_i64(pl.chunk), _i32(pl.bucket_of), _i64(pl.bucket_off), _i32(pl.bucket_dtype),
             _i32([p.shard_dtype for p in pl.params])]
     _load().oracle_reduce_scatter_copy_out(len(pl.params), *(a.ctypes.data for a in keep), _ptrs(rows), _ptrs(out))
+    return out
+
+
+def emulated_reduce_scatter(pl: Plan, packed):
+    """packed[q] = rank q's bucket buffers (as from pack_reduce_scatter).
+    Returns, per bucket, the [W * S_b] elementwise sum over ranks in rank
+    order; row r is rank r's reduce-scatter output."""
+    out = []
+    for b, (dt, S) in enumerate(zip(pl.bucket_dtype, pl.bucket_S)):
+        ins = [np.ascontiguousarray(packed[q][b]).reshape(-1) for q in range(len(packed))]
+        for x in ins:
+            _check(x, dt, pl.W * S, "packed buffer")
+        res = np.empty(pl.W * S, DTYPE_NP[dt])
+        if ins:
+            _load().oracle_emulated_reduce_scatter(res.size, dt, len(ins), _ptrs(ins), res.ctypes.data)
+        out.append(res)
     return out
 
 

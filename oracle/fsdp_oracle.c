@@ -306,3 +306,49 @@ void oracle_reduce_scatter_copy_out(int32_t n_params, const int64_t *chunk, cons
       cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);
   }
 }
+
+/* ---------------------------------------------------------------------------
+ * Emulated reduce-scatter on one device (a test utility, not a collective).
+ * Every rank's packed bucket buffer has the same [W, S_b] shape, and rank r's
+ * reduce-scatter output is row r of their elementwise sum ([Unit]
+ * collective-count section: the gradient is reduced across ranks and
+ * scattered so every rank keeps its own slice).  The sum runs over ranks
+ * q = 0, 1, ..., W-1 in that order, each partial sum rounded to the bucket
+ * dtype ("Training frameworks" note, "Check the objective before measuring
+ * speed": reduction order changes results, so the order is fixed):
+ *   FP32: acc = in_0[i]; acc = fl32(acc + in_q[i])
+ *   BF16: acc = in_0[i]; acc = rne_bf16(fl32(f32(acc) + f32(in_q[i])))
+ * where fl32 is one IEEE-754 binary32 addition rounded to nearest even.
+ * Inputs are expected finite (a NaN's payload after an addition is not
+ * specified by IEEE-754).
+ * ------------------------------------------------------------------------ */
+static float f32_of_bits(uint32_t u) {
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static uint32_t bits_of_f32(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return u;
+}
+
+void oracle_emulated_reduce_scatter(int64_t n, int32_t dtype, int32_t n_inputs, const void *const *inputs,
+                                    void *out) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (dtype == ORACLE_F32) {
+      volatile float acc = f32_of_bits(((const uint32_t *)inputs[0])[i]);
+      for (int32_t q = 1; q < n_inputs; ++q) acc = acc + f32_of_bits(((const uint32_t *)inputs[q])[i]);
+      ((uint32_t *)out)[i] = bits_of_f32(acc);
+    } else {
+      uint16_t acc = ((const uint16_t *)inputs[0])[i];
+      for (int32_t q = 1; q < n_inputs; ++q) {
+        volatile float sum = f32_of_bits(oracle_bf16_to_f32(acc)) +
+                             f32_of_bits(oracle_bf16_to_f32(((const uint16_t *)inputs[q])[i]));
+        acc = oracle_f32_to_bf16(bits_of_f32(sum));
+      }
+      ((uint16_t *)out)[i] = acc;
+    }
+  }
+}

@@ -58,6 +58,12 @@ MUTANTS = {
     "rs copy-out: cast to the reduce dtype":
         ("cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);",
          "cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], bucket_dtype[b], i);"),
+    "emulated rs: ranks summed in reverse order":
+        ("for (int32_t q = 1; q < n_inputs; ++q) acc = acc + f32_of_bits(((const uint32_t *)inputs[q])[i]);",
+         "for (int32_t q = n_inputs - 1; q >= 1; --q) acc = acc + f32_of_bits(((const uint32_t *)inputs[q])[i]);"),
+    "emulated rs: bf16 partial sums not rounded":
+        ("        acc = oracle_f32_to_bf16(bits_of_f32(sum));\n      }\n      ((uint16_t *)out)[i] = acc;",
+         "        acc = (uint16_t)(bits_of_f32(sum) >> 16);\n      }\n      ((uint16_t *)out)[i] = acc;"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and callable(getattr(pins, n))]

@@ -606,3 +606,67 @@ def test_row_mode_linear_examples():
     assert plan([Param(36)], 4).chunk == [9]
     # Linear(3, 3) at W = 4: one row per rank in row mode, 4 rows = 12 slots.
     assert plan([Param(9)], 4, row_elems=[3]).chunk == [3]
+
+
+# ---------------------------------------------------------------------------
+# Emulated reduce-scatter: sum over ranks in rank order, rounded per add.
+# ---------------------------------------------------------------------------
+def _ers(dt, rows):
+    pl = plan([Param(len(rows[0]), dt, dt)], 1)
+    return oracle.emulated_reduce_scatter(pl, [[np.asarray(r, NP[dt])] for r in rows])[0]
+
+
+def f32b(*vals):
+    return np.array(vals, np.float32).view(np.uint32)
+
+
+def test_emulated_rs_textbook_sums():
+    # one rank: identity
+    x = f32b(1.5, -0.0, 3e-45, 7.0)
+    assert np.array_equal(_ers(F32, [x]), x)
+    # small integers add exactly in any order
+    rng = np.random.default_rng(3)
+    ints = rng.integers(-1000, 1000, (8, 50))
+    got = _ers(F32, [f32b(*row) for row in ints])
+    assert np.array_equal(got.view(np.float32), ints.sum(0).astype(np.float32))
+    # order matters, and it is rank order: (1 + 2^24) rounds to 2^24 (tie to
+    # even) before -2^24 is added, while 2^24 - 2^24 + 1 = 1
+    assert _ers(F32, [f32b(1.0), f32b(2.0**24), f32b(-(2.0**24))]).view(np.float32)[0] == 0.0
+    assert _ers(F32, [f32b(2.0**24), f32b(-(2.0**24)), f32b(1.0)]).view(np.float32)[0] == 1.0
+    # subnormals are kept: 2 * smallest subnormal
+    assert _ers(F32, [np.array([1], np.uint32), np.array([1], np.uint32)])[0] == 2
+
+
+def test_emulated_rs_bf16_rounds_every_partial_sum():
+    one, tiny = 0x3F80, 0x3B80                 # 1.0 and 2^-8 in BF16
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even -> 1.0, every time
+    assert _ers(BF16, [np.array([one]), np.array([tiny]), np.array([tiny])])[0] == one
+    # 2^-8 + 2^-8 = 2^-7 first, then 1 + 2^-7 is exact: 0x3F81
+    assert _ers(BF16, [np.array([tiny]), np.array([tiny]), np.array([one])])[0] == 0x3F81
+
+
+def test_emulated_rs_matches_sequential_float32_and_pack_composition():
+    rng = np.random.default_rng(47)
+    params = [Param(37, BF16, F32, F32), Param(20, F32, BF16, BF16), Param(64, F32, F32, BF16)]
+    W = 4
+    pl = plan(params, W)
+    grads = [[rand_bits(rng, p.numel, p.grad_dtype) for p in params] for _ in range(W)]
+    packed = [oracle.pack_reduce_scatter(pl, grads[q]) for q in range(W)]
+    summed = oracle.emulated_reduce_scatter(pl, packed)
+    for b, dt in enumerate(pl.bucket_dtype):
+        if dt == F32:
+            acc = packed[0][b].view(np.float32).copy()
+            for q in range(1, W):
+                acc = (acc + packed[q][b].view(np.float32)).astype(np.float32)
+            assert np.array_equal(summed[b], acc.view(np.uint32))
+        else:
+            acc = torch_cast(packed[0][b], BF16, F32).view(np.float32)
+            for q in range(1, W):
+                s = (acc + torch_cast(packed[q][b], BF16, F32).view(np.float32)).astype(np.float32)
+                acc = torch_cast(torch_cast(s.view(np.uint32), F32, BF16), BF16, F32).view(np.float32)
+            assert np.array_equal(summed[b], torch_cast(acc.view(np.uint32), F32, BF16))
+    # rank r's sharded gradients after the emulated reduce-scatter
+    for r in range(W):
+        rows = [buf[r * S:(r + 1) * S] for buf, S in zip(summed, pl.bucket_S)]
+        shards = oracle.reduce_scatter_copy_out(pl, rows)
+        assert [s.size for s in shards] == pl.chunk
