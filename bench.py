@@ -60,6 +60,7 @@ FALLBACK_HBM_GBS = 6800.0
 ESZ = {"f32": 4, "bf16": 2}
 STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
 STEP_RS = " + reduce-scatter copy-out (row 0 of each bucket as this rank's reduced row)"
+STEP_ERS = " + emulated reduce-scatter after the pack (this rank's buckets + W-1 other ranks' buffers)"
 WORKLOADS = {
     # name: (factory, description); the first is the benchmark's workload.
     "mixed50m": (lambda: wl.mixed_50m(W=8),
@@ -93,6 +94,8 @@ def parse_args(argv=None):
                     help="layout to time (the benchmark's metric is quoted on mixed50m)")
     ap.add_argument("--rs-copy-out", action="store_true",
                     help="add the reduce-scatter copy-out (reduced rows to sharded gradients) to every step")
+    ap.add_argument("--emulated-rs", action="store_true",
+                    help="add the emulated reduce-scatter (sum of W ranks' packed buffers) after the pack")
     ap.add_argument("--batched", action="store_true",
                     help="one launch per operation for all of the workload's groups (*_batched entry points)")
     return ap.parse_args(argv)
@@ -145,7 +148,9 @@ def op_bytes(specs, W, bucket_bytes, S_ag):
     copy_in = sum(ci * ESZ[s.shard_dtype] for ci, s in zip(c, specs)) + S_ag
     copy_out = 2 * sum(s.numel * ESZ[s.param_dtype] for s in specs)
     rs_copy_out = sum(ci * (ESZ[s.reduce_dtype] + ESZ[s.shard_dtype]) for ci, s in zip(c, specs))
-    return {"pack": pack, "copy_in": copy_in, "copy_out": copy_out, "rs_copy_out": rs_copy_out}
+    emulated_rs = (W + 1) * sum(bucket_bytes)   # W packed buffers read, one reduced buffer written
+    return {"pack": pack, "copy_in": copy_in, "copy_out": copy_out, "rs_copy_out": rs_copy_out,
+            "emulated_rs": emulated_rs}
 
 
 def read_peaks():
@@ -356,7 +361,7 @@ def cpu_baseline(sampler: OracleSampler, seconds: float) -> dict:
 class DeviceSet:
     """One complete set of device buffers for a step (two sets rotate)."""
 
-    def __init__(self, fp, torch, L, specs, W, info, host_grads, host_shards, rank_row):
+    def __init__(self, fp, torch, L, specs, W, info, host_grads, host_shards, rank_row, others=None):
         dev = torch.device("cuda")
         c = chunks(specs, W)
         self.S_ag = info.ag_bytes
@@ -378,9 +383,19 @@ class DeviceSet:
         foffs, ftot = flat_offsets(f_sizes)
         self.full = torch.empty(ftot, dtype=torch.uint8, device=dev)
         self.full_ptrs = fp.pointer_array([self.full.data_ptr() + o for o in foffs])
-        # Reduce-scatter copy-out: row 0 of each bucket stands for this
-        # rank's reduced row; the sharded gradients go to their own buffer.
-        self.row0_ptrs = fp.pointer_array([b.data_ptr() for b in self.buckets])
+        # Emulated reduce-scatter: this rank's buckets plus the other W - 1
+        # ranks' buffers (`others[b]`, shared by both sets) summed into
+        # `reduced`; the reduce-scatter copy-out then reads row 0 of it.
+        self.reduced = None
+        if others is not None:
+            self.reduced = [torch.empty_like(b) for b in self.buckets]
+            self.packed_ptrs = fp.pointer_array([p for b, mine in enumerate(self.buckets)
+                                                 for p in [mine.data_ptr()] + [o.data_ptr() for o in others[b]]])
+            self.reduced_ptrs = fp.pointer_array(self.reduced)
+        # Reduce-scatter copy-out: row 0 of each bucket (or of the reduced
+        # buffer) stands for this rank's reduced row; the sharded gradients
+        # go to their own buffer.
+        self.row0_ptrs = fp.pointer_array([b.data_ptr() for b in (self.reduced or self.buckets)])
         h_sizes = [ci * ESZ[s.shard_dtype] for ci, s in zip(c, specs)]
         hoffs, htot = flat_offsets(h_sizes)
         self.sharded = torch.empty(htot, dtype=torch.uint8, device=dev)
@@ -396,34 +411,46 @@ class DeviceSet:
             del other
 
     def step(self, fp, L, h, ev=None, rs=False):
-        if ev is not None:
-            ev[0].record()
+        """pack, [emulated reduce-scatter], copy-in, copy-out, [rs copy-out];
+        ev[k] is recorded after the k-th launch (ev[0] before the first)."""
+        k = 0
+
+        def mark():
+            nonlocal k
+            if ev is not None:
+                ev[k].record()
+            k += 1
+        mark()
         fp.fsdp_pack_reduce_scatter(L, self.grad_ptrs, self.bucket_ptrs, h)
-        if ev is not None:
-            ev[1].record()
+        mark()
+        if self.reduced is not None:
+            fp.fsdp_emulated_reduce_scatter(L, self.packed_ptrs, self.reduced_ptrs, h)
+            mark()
         fp.fsdp_allgather_copy_in(L, self.shard_ptrs, self.row_ptr, h)
-        if ev is not None:
-            ev[2].record()
+        mark()
         fp.fsdp_allgather_copy_out(L, self.gathered.data_ptr(), self.full_ptrs, h)
-        if ev is not None:
-            ev[3].record()
+        mark()
         if rs:
             fp.fsdp_reduce_scatter_copy_out(L, self.row0_ptrs, self.sharded_ptrs, h)
-            if ev is not None:
-                ev[4].record()
+            mark()
 
 
 class Group:
     """One fully_shard group on the device: its layout and two buffer sets."""
 
-    def __init__(self, fp, torch, work, g, inputs):
+    def __init__(self, fp, torch, work, g, inputs, emulated_rs=False):
         self.specs = work.groups[g]
         self.L = fp.fsdp_plan_layout(self.specs, work.W)
         self.info = fp.fsdp_layout_query(self.L)
         bucket_bytes = [fp.fsdp_layout_bucket(self.L, b).bytes for b in range(self.info.n_buckets)]
         self.nbytes = op_bytes(self.specs, work.W, bucket_bytes, self.info.ag_bytes)
         grads, shards = inputs
-        self.sets = [DeviceSet(fp, torch, self.L, self.specs, work.W, self.info, grads, shards, 0) for _ in range(2)]
+        others = None
+        if emulated_rs:   # the other ranks' packed buffers (contents do not matter for timing)
+            others = [[torch.zeros(n, dtype=torch.uint8, device="cuda") for _ in range(work.W - 1)]
+                      for n in bucket_bytes]
+        self.sets = [DeviceSet(fp, torch, self.L, self.specs, work.W, self.info, grads, shards, 0, others)
+                     for _ in range(2)]
 
 
 class Batch:
@@ -482,8 +509,11 @@ def run_ours(args):
     factory, description = WORKLOADS[args.workload]
     work = factory()
     inputs = [host_inputs(work, g) for g in range(len(work.groups))]
-    groups = [Group(fp, torch, work, g, inputs[g]) for g in range(len(work.groups))]
-    OPS = ("pack", "copy_in", "copy_out") + (("rs_copy_out",) if args.rs_copy_out else ())
+    groups = [Group(fp, torch, work, g, inputs[g], args.emulated_rs) for g in range(len(work.groups))]
+    if args.batched and args.emulated_rs:
+        raise SystemExit("--emulated-rs has no batched form; drop --batched")
+    OPS = (("pack",) + (("emulated_rs",) if args.emulated_rs else ()) + ("copy_in", "copy_out")
+           + (("rs_copy_out",) if args.rs_copy_out else ()))
     nbytes = {k: sum(grp.nbytes[k] for grp in groups) for k in OPS}
     step_bytes = sum(nbytes.values())
     h = torch.cuda.current_stream().cuda_stream
@@ -594,7 +624,8 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "bf16+f32",
             "data": "synthetic",
-            "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else ""), "world_size_layout": work.W,
+            "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else "")
+                       + (STEP_ERS if args.emulated_rs else ""), "world_size_layout": work.W,
                        "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
                        "parallelism": f"replicas x{world} (no data-path collective)",
                        "l2": "inputs larger than L2: two rotating buffer sets of "

@@ -560,6 +560,98 @@ fsdp_status_t batch_launch(const fsdp_layout *const *Ls, int n, Op op, const voi
 }
 
 // ---------------------------------------------------------------------------
+// Emulated reduce-scatter (a test utility): out[i] = in_0[i] + in_1[i] + ...
+// added over the inputs in order, each partial sum rounded to the element
+// type -- FP32: one correctly rounded binary32 addition (no flush of
+// subnormals); BF16: a binary32 addition of the two values, then round to
+// nearest even to BF16; a NaN sum is the canonical quiet NaN.  The first
+// input enters unchanged.  Every input and the output have the same shape.
+// ---------------------------------------------------------------------------
+constexpr int kMaxSumInputs = 256;
+constexpr int kSumThreads = 256;
+
+struct SumArgs {
+  const void *in[kMaxSumInputs];
+  void *out;
+  int64_t n;      // elements
+  int32_t n_in;
+  int32_t head;   // leading elements before the first 16-byte boundary; -1: no vector path
+};
+
+// A NaN sum (a NaN operand, or infinities of opposite sign) becomes the
+// canonical quiet NaN, so the result does not depend on the machine.
+template <bool BF16>
+__device__ __forceinline__ uint32_t add_bits(uint32_t acc, uint32_t x) {
+  if constexpr (BF16) {
+    const float s = __fadd_rn(__uint_as_float(acc << 16), __uint_as_float(x << 16));
+    return (s != s) ? 0x7FC0u : f32_to_bf16_bits(__float_as_uint(s));
+  } else {
+    const float s = __fadd_rn(__uint_as_float(acc), __uint_as_float(x));
+    return (s != s) ? 0x7FC00000u : __float_as_uint(s);
+  }
+}
+
+// Lane-wise sum of two 16-byte vectors of elements.
+template <bool BF16>
+__device__ __forceinline__ uint4 add_vec(uint4 a, uint4 b) {
+  if constexpr (BF16) {
+    auto pair = [](uint32_t x, uint32_t y) {
+      return add_bits<true>(x & 0xFFFFu, y & 0xFFFFu) | (add_bits<true>(x >> 16, y >> 16) << 16);
+    };
+    return make_uint4(pair(a.x, b.x), pair(a.y, b.y), pair(a.z, b.z), pair(a.w, b.w));
+  } else {
+    return make_uint4(add_bits<false>(a.x, b.x), add_bits<false>(a.y, b.y), add_bits<false>(a.z, b.z),
+                      add_bits<false>(a.w, b.w));
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void sum_scalar(const SumArgs &a, int64_t i) {
+  if constexpr (BF16) {
+    uint32_t acc = reinterpret_cast<const uint16_t *>(a.in[0])[i];
+    for (int q = 1; q < a.n_in; ++q) acc = add_bits<true>(acc, reinterpret_cast<const uint16_t *>(a.in[q])[i]);
+    reinterpret_cast<uint16_t *>(a.out)[i] = (uint16_t)acc;
+  } else {
+    uint32_t acc = reinterpret_cast<const uint32_t *>(a.in[0])[i];
+    for (int q = 1; q < a.n_in; ++q) acc = add_bits<false>(acc, reinterpret_cast<const uint32_t *>(a.in[q])[i]);
+    reinterpret_cast<uint32_t *>(a.out)[i] = acc;
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kSumThreads) sum_kernel(const __grid_constant__ SumArgs a) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if (a.head < 0) {
+    for (int64_t i = tid; i < a.n; i += stride) sum_scalar<BF16>(a, i);
+    return;
+  }
+  constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
+  const int64_t head = a.head < a.n ? a.head : a.n;
+  const int64_t nvec = (a.n - head) / EPV;
+  const int64_t tail0 = head + nvec * EPV;
+  if (tid < head) sum_scalar<BF16>(a, tid);
+  if (tail0 + tid < a.n) sum_scalar<BF16>(a, tail0 + tid);
+  const int es = BF16 ? 2 : 4;
+  for (int64_t v = tid; v < nvec; v += stride) {
+    const int64_t byte = (head + v * EPV) * es;
+    uint4 acc = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(a.in[0]) + byte));
+    int q = 1;
+    for (; q + 3 < a.n_in; q += 4) {  // four independent loads in flight, added in order
+      uint4 x[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        x[k] = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(a.in[q + k]) + byte));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc = add_vec<BF16>(acc, x[k]);
+    }
+    for (; q < a.n_in; ++q)
+      acc = add_vec<BF16>(acc, __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(a.in[q]) + byte)));
+    *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(a.out) + byte) = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host-side argument checks (nothing is launched unless all pass).
 // ---------------------------------------------------------------------------
 fsdp_status_t check_layout(const fsdp_layout *L) {
@@ -677,6 +769,7 @@ fsdp_status_t device_setup(fsdp_layout *L) {
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("device query failed: ") + cudaGetErrorString(e));
   const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
   L->resident = resident;
+  L->sms = sms;
   for (int op = 0; op < OP_COUNT; ++op) {
     int64_t g = L->op[op].count < resident ? L->op[op].count : resident;
     L->op[op].grid = (int32_t)(g > 0 ? g : 0);
@@ -932,6 +1025,50 @@ fsdp_status_t fsdp_reduce_scatter_copy_out_batched(const fsdp_layout_t *const *l
   }
   return batch_launch(layouts, n_layouts, OP_RS_COPY_OUT, ptrs, (int)at, base,
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+fsdp_status_t fsdp_emulated_reduce_scatter(const fsdp_layout_t *L, const void *const *packed,
+                                           void *const *reduced, fsdp_stream_t stream) {
+  fsdp_status_t st = check_layout(L);
+  if (st != FSDP_OK) return st;
+  const int B = (int)L->bucket.size(), W = L->W;
+  if (W > kMaxSumInputs) return fail(FSDP_EUNSUPPORTED, "emulated reduce-scatter supports W <= 256");
+  if (B > 0 && (!packed || !reduced)) return fail(FSDP_EINVAL, "packed or reduced is NULL");
+  for (int b = 0; b < B; ++b) {
+    const int64_t sz = dtype_bytes(L->bucket[b].dtype), bytes = (int64_t)W * L->bucket[b].S * sz;
+    for (int q = 0; q < W; ++q)
+      if ((st = check_ptr(packed[(int64_t)b * W + q], bytes, sz, "packed", (int64_t)b * W + q)) != FSDP_OK) return st;
+    if ((st = check_ptr(reduced[b], bytes, sz, "reduced", b)) != FSDP_OK) return st;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int b = 0; b < B; ++b) {
+    const int64_t n = (int64_t)W * L->bucket[b].S;
+    if (n == 0) continue;
+    const int sz = (int)dtype_bytes(L->bucket[b].dtype);
+    SumArgs a;
+    a.out = reduced[b];
+    a.n = n;
+    a.n_in = W;
+    // The vector path needs every pointer at the same phase modulo 16 bytes.
+    const uintptr_t phase = (uintptr_t)reduced[b] & 15u;
+    bool same = true;
+    for (int q = 0; q < W; ++q) {
+      a.in[q] = packed[(int64_t)b * W + q];
+      same = same && (((uintptr_t)a.in[q] & 15u) == phase);
+    }
+    a.head = same ? (int32_t)(((16u - phase) & 15u) / (unsigned)sz) : -1;
+    const int64_t work = same ? n / (16 / sz) + 1 : n;
+    int64_t grid = (work + kSumThreads - 1) / kSumThreads;
+    const int64_t cap = (int64_t)(L->sms > 0 ? L->sms : 1) * 8;
+    if (grid > cap) grid = cap;
+    void *args[] = {&a};
+    const void *fn = sz == 2 ? reinterpret_cast<const void *>(&sum_kernel<true>)
+                             : reinterpret_cast<const void *>(&sum_kernel<false>);
+    cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kSumThreads), args, 0, s);
+    if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  }
+  clear_error();
+  return FSDP_OK;
 }
 
 fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream) {

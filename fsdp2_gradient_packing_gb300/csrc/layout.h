@@ -92,6 +92,7 @@ struct fsdp_layout {
   std::vector<fsdp::WorkItem> items;   // pack, copy-in, copy-out, rs copy-out tables back to back
   fsdp::OpTable op[fsdp::OP_COUNT];
   int64_t resident = 0;                // CTAs a launch keeps resident on the device
+  int32_t sms = 0;                     // SMs of the device
   fsdp::WorkItem *d_items = nullptr;   // device copy of `items`
   uint32_t *d_status = nullptr;        // device status word (bounded-wait failures)
 };

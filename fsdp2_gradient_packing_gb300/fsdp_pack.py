@@ -83,6 +83,7 @@ _SIGNATURES = {
     "fsdp_allgather_copy_in": (_ST, [_LAYOUT, ctypes.POINTER(_P), _P, _P]),
     "fsdp_allgather_copy_out": (_ST, [_LAYOUT, _P, ctypes.POINTER(_P), _P]),
     "fsdp_reduce_scatter_copy_out": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "fsdp_emulated_reduce_scatter": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_reduce_scatter_copy_out_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
                                                    ctypes.POINTER(_P), _P]),
     "fsdp_pack_reduce_scatter_batched": (_ST, [ctypes.POINTER(_LAYOUT), ctypes.c_int32, ctypes.POINTER(_P),
@@ -272,6 +273,13 @@ def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None)
 def fsdp_reduce_scatter_copy_out(layout: Layout, reduced_rows, sharded_grads, stream=None) -> None:
     _check(_lib.fsdp_reduce_scatter_copy_out(layout.handle, pointer_array(reduced_rows), pointer_array(sharded_grads),
                                              _stream(stream)), "fsdp_reduce_scatter_copy_out")
+
+
+def fsdp_emulated_reduce_scatter(layout: Layout, packed, reduced, stream=None) -> None:
+    """packed: n_buckets * W pointers, bucket-major (packed[b*W + q] = rank q's
+    bucket b); reduced: one [W, S_b] buffer per bucket."""
+    _check(_lib.fsdp_emulated_reduce_scatter(layout.handle, pointer_array(packed), pointer_array(reduced),
+                                             _stream(stream)), "fsdp_emulated_reduce_scatter")
 
 
 def layout_array(layouts):

@@ -199,8 +199,10 @@ BF16_SPECIALS = np.array([
 ], dtype=np.uint16)
 
 
-def inject_specials(bits: np.ndarray, dtype: str, frac: float, seed: int, *key: int) -> np.ndarray:
-    """Overwrite a seeded fraction of ``bits`` (in place) with special patterns."""
+def inject_specials(bits: np.ndarray, dtype: str, frac: float, seed: int, *key: int,
+                    finite: bool = False) -> np.ndarray:
+    """Overwrite a seeded fraction of ``bits`` (in place) with special patterns
+    (only the finite ones if ``finite``)."""
     n = bits.size
     if n == 0 or frac <= 0:
         return bits
@@ -208,6 +210,9 @@ def inject_specials(bits: np.ndarray, dtype: str, frac: float, seed: int, *key: 
     k = max(1, int(n * frac))
     pos = rng.choice(n, size=min(k, n), replace=False)
     pool = F32_SPECIALS if dtype == "f32" else BF16_SPECIALS
+    if finite:
+        exp_mask = np.uint32(0x7F800000) if dtype == "f32" else np.uint16(0x7F80)
+        pool = pool[(pool & exp_mask) != exp_mask]
     bits.reshape(-1)[pos] = pool[rng.integers(0, pool.size, size=pos.size)]
     return bits
 

@@ -259,6 +259,33 @@ fsdp_status_t fsdp_reduce_scatter_copy_out(const fsdp_layout_t *L, const void *c
                                            void *const *sharded_grads, fsdp_stream_t stream);
 
 /*
+ * Emulated reduce-scatter on one device: a test and benchmarking utility that
+ * stands in for the collective, so that pack -> reduce-scatter -> copy-out
+ * can run end to end without a network.  It is not a collective and moves no
+ * data between devices.  Every rank's packed bucket buffer has the same
+ * [W, S_b] shape and rank r's reduce-scatter output is row r of their
+ * elementwise sum ([Unit], collective-count section).  The sum runs over
+ * ranks q = 0, 1, ..., W-1 in that order with every partial sum rounded to
+ * the bucket dtype: FP32, one IEEE binary32 addition rounded to nearest even
+ * (subnormals kept); BF16, a binary32 addition of the two values, then round
+ * to nearest even to BF16.  A NaN sum (a NaN operand, or infinities of
+ * opposite sign) is the canonical quiet NaN 0x7FC00000 / 0x7FC0; rank 0's
+ * value enters unchanged.  A fixed order makes the result reproducible bit
+ * for bit ("Training frameworks" note, "Check the objective before measuring
+ * speed": reduction order changes results).
+ *   packed:  host array of n_buckets * W device pointers, bucket-major:
+ *            packed[b*W + q] is rank q's buffer of bucket b (W*S_b elements).
+ *   reduced: host array of n_buckets device pointers, W*S_b elements each;
+ *            row r receives rank r's reduce-scatter output.  Must not
+ *            overlap the inputs.
+ * W <= 256 (FSDP_EUNSUPPORTED above).  One launch per non-empty bucket; 16-
+ * byte vectors when every pointer has the same address modulo 16, element by
+ * element otherwise.
+ */
+fsdp_status_t fsdp_emulated_reduce_scatter(const fsdp_layout_t *L, const void *const *packed,
+                                           void *const *reduced, fsdp_stream_t stream);
+
+/*
  * Batched calls: the work of several layouts (for instance every
  * fully_shard group of a model, one per transformer block) in ONE kernel
  * launch, with the same results as calling the single entry point once per

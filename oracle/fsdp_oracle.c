@@ -318,9 +318,12 @@ void oracle_reduce_scatter_copy_out(int32_t n_params, const int64_t *chunk, cons
  * speed": reduction order changes results, so the order is fixed):
  *   FP32: acc = in_0[i]; acc = fl32(acc + in_q[i])
  *   BF16: acc = in_0[i]; acc = rne_bf16(fl32(f32(acc) + f32(in_q[i])))
- * where fl32 is one IEEE-754 binary32 addition rounded to nearest even.
- * Inputs are expected finite (a NaN's payload after an addition is not
- * specified by IEEE-754).
+ * where fl32 is one IEEE-754 binary32 addition rounded to nearest even.  A
+ * sum that is NaN (a NaN operand, or infinities of opposite sign) is the
+ * canonical quiet NaN 0x7FC00000 (FP32) / 0x7FC0 (BF16): IEEE-754 leaves the
+ * payload of such a result open, and fixing it makes the result the same on
+ * every machine.  The first rank's value enters unchanged (with one rank
+ * there is no addition and the output is the input, bit for bit).
  * ------------------------------------------------------------------------ */
 static float f32_of_bits(uint32_t u) {
   float f;
@@ -334,19 +337,26 @@ static uint32_t bits_of_f32(float f) {
   return u;
 }
 
+/* One binary32 addition, a NaN result made canonical. */
+static float add_f32(float a, float b) {
+  volatile float s = a + b;
+  if (s != s) return f32_of_bits(0x7FC00000u);
+  return s;
+}
+
 void oracle_emulated_reduce_scatter(int64_t n, int32_t dtype, int32_t n_inputs, const void *const *inputs,
                                     void *out) {
   for (int64_t i = 0; i < n; ++i) {
     if (dtype == ORACLE_F32) {
-      volatile float acc = f32_of_bits(((const uint32_t *)inputs[0])[i]);
-      for (int32_t q = 1; q < n_inputs; ++q) acc = acc + f32_of_bits(((const uint32_t *)inputs[q])[i]);
+      float acc = f32_of_bits(((const uint32_t *)inputs[0])[i]);
+      for (int32_t q = 1; q < n_inputs; ++q) acc = add_f32(acc, f32_of_bits(((const uint32_t *)inputs[q])[i]));
       ((uint32_t *)out)[i] = bits_of_f32(acc);
     } else {
       uint16_t acc = ((const uint16_t *)inputs[0])[i];
       for (int32_t q = 1; q < n_inputs; ++q) {
-        volatile float sum = f32_of_bits(oracle_bf16_to_f32(acc)) +
-                             f32_of_bits(oracle_bf16_to_f32(((const uint16_t *)inputs[q])[i]));
-        acc = oracle_f32_to_bf16(bits_of_f32(sum));
+        float sum = add_f32(f32_of_bits(oracle_bf16_to_f32(acc)),
+                            f32_of_bits(oracle_bf16_to_f32(((const uint16_t *)inputs[q])[i])));
+        acc = (sum != sum) ? (uint16_t)0x7FC0 : oracle_f32_to_bf16(bits_of_f32(sum));
       }
       ((uint16_t *)out)[i] = acc;
     }

@@ -3,7 +3,8 @@
 Each case below plants one mistake (a dropped term, an off-by-one index, a
 wrong comparison, a lost bit) in a temporary copy of ``oracle/fsdp_oracle.c``,
 builds it, swaps it in for the real oracle library, and re-runs the pins of
-tests/test_oracle_pins.py.  At least one pin must fail for every mutant.
+tests/test_oracle_pins.py.  The mutants run in this process, so every one of
+them keeps all its memory accesses inside the buffers it is given.  At least one pin must fail for every mutant.
 Everything runs on the CPU; the mistakes are planted in the oracle only.
 """
 import ctypes
@@ -55,15 +56,18 @@ MUTANTS = {
     "rs copy-out: bucket offset dropped":
         ("cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);",
          "cast_element(rows[b], bucket_dtype[b], i, sharded[p], shard_dtype[p], i);"),
-    "rs copy-out: cast to the reduce dtype":
-        ("cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], shard_dtype[p], i);",
-         "cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i, sharded[p], bucket_dtype[b], i);"),
+    "rs copy-out: last slot of every chunk skipped":
+        ("    for (int64_t i = 0; i < chunk[p]; ++i)\n      cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i",
+         "    for (int64_t i = 0; i < chunk[p] - 1; ++i)\n      cast_element(rows[b], bucket_dtype[b], bucket_off[p] + i"),
     "emulated rs: ranks summed in reverse order":
-        ("for (int32_t q = 1; q < n_inputs; ++q) acc = acc + f32_of_bits(((const uint32_t *)inputs[q])[i]);",
-         "for (int32_t q = n_inputs - 1; q >= 1; --q) acc = acc + f32_of_bits(((const uint32_t *)inputs[q])[i]);"),
+        ("for (int32_t q = 1; q < n_inputs; ++q) acc = add_f32(acc, f32_of_bits(((const uint32_t *)inputs[q])[i]));",
+         "for (int32_t q = n_inputs - 1; q >= 1; --q) acc = add_f32(acc, f32_of_bits(((const uint32_t *)inputs[q])[i]));"),
     "emulated rs: bf16 partial sums not rounded":
-        ("        acc = oracle_f32_to_bf16(bits_of_f32(sum));\n      }\n      ((uint16_t *)out)[i] = acc;",
-         "        acc = (uint16_t)(bits_of_f32(sum) >> 16);\n      }\n      ((uint16_t *)out)[i] = acc;"),
+        ("acc = (sum != sum) ? (uint16_t)0x7FC0 : oracle_f32_to_bf16(bits_of_f32(sum));",
+         "acc = (sum != sum) ? (uint16_t)0x7FC0 : (uint16_t)(bits_of_f32(sum) >> 16);"),
+    "emulated rs: NaN sums keep a machine payload":
+        ("  if (s != s) return f32_of_bits(0x7FC00000u);\n  return s;",
+         "  return s;"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and callable(getattr(pins, n))]

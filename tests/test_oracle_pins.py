@@ -637,6 +637,20 @@ def test_emulated_rs_textbook_sums():
     assert _ers(F32, [np.array([1], np.uint32), np.array([1], np.uint32)])[0] == 2
 
 
+def test_emulated_rs_nan_sums_are_canonical():
+    inf, ninf = 0x7F800000, 0xFF800000
+    assert _ers(F32, [np.array([inf], np.uint32), np.array([ninf], np.uint32)])[0] == 0x7FC00000
+    payload = 0xFFA12345                       # negative signalling NaN with a payload
+    assert _ers(F32, [np.array([payload], np.uint32), np.array([0x3F800000], np.uint32)])[0] == 0x7FC00000
+    assert _ers(F32, [np.array([0x3F800000], np.uint32), np.array([payload], np.uint32)])[0] == 0x7FC00000
+    assert _ers(F32, [np.array([payload], np.uint32)])[0] == payload   # one rank: no addition
+    assert _ers(BF16, [np.array([0x7F80]), np.array([0xFF80])])[0] == 0x7FC0
+    assert _ers(BF16, [np.array([0xFFA1]), np.array([0x3F80])])[0] == 0x7FC0
+    # -0 survives when nothing is added, and -0 + -0 = -0
+    assert _ers(F32, [np.array([0x80000000], np.uint32)])[0] == 0x80000000
+    assert _ers(F32, [np.array([0x80000000], np.uint32)] * 2)[0] == 0x80000000
+
+
 def test_emulated_rs_bf16_rounds_every_partial_sum():
     one, tiny = 0x3F80, 0x3B80                 # 1.0 and 2^-8 in BF16
     # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even -> 1.0, every time
@@ -651,6 +665,8 @@ def test_emulated_rs_matches_sequential_float32_and_pack_composition():
     W = 4
     pl = plan(params, W)
     grads = [[rand_bits(rng, p.numel, p.grad_dtype) for p in params] for _ in range(W)]
+    # finite inputs only here: numpy keeps a NaN operand's payload, the
+    # definition does not
     packed = [oracle.pack_reduce_scatter(pl, grads[q]) for q in range(W)]
     summed = oracle.emulated_reduce_scatter(pl, packed)
     for b, dt in enumerate(pl.bucket_dtype):

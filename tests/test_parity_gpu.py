@@ -152,6 +152,61 @@ def test_row_chunk_mode_batched(fp):
             run.close()
 
 
+def _end_to_end(fp, specs, W, work, seed, same_phase):
+    """W ranks: pack each rank's gradients, emulated reduce-scatter, then each
+    rank's reduce-scatter copy-out -- all on the GPU, against the oracle."""
+    rng = np.random.default_rng(seed)
+    pl = oracle.plan(oracle.params_from_specs(specs), W)
+    grads = []
+    for q in range(W):
+        row = []
+        for i, s in enumerate(specs):
+            bits = wl.normal_bits(s.numel, s.grad_dtype, work.std, work.seed, 0, i, 20 + q)
+            wl.inject_specials(bits, s.grad_dtype, 0.05, work.seed, 0, i, 20 + q)
+            row.append(bits)
+        grads.append(row)
+    rho = ["f32" if d == oracle.F32 else "bf16" for d in pl.bucket_dtype]
+    phase = {r: int(rng.integers(0, 16 // ESZ[r])) * ESZ[r] for r in ("f32", "bf16")}
+    off = (lambda r: phase[r]) if same_phase else (lambda r: int(rng.integers(0, 16 // ESZ[r])) * ESZ[r])
+    with fp.fsdp_plan_layout(specs, W) as L:
+        packed, keep = [], []
+        for q in range(W):
+            g = [DevBuf(x.nbytes, 0, x) for x in grads[q]]
+            out = [DevBuf(W * S * ESZ[r], off(r)) for r, S in zip(rho, pl.bucket_S)]
+            fp.fsdp_pack_reduce_scatter(L, [b.ptr for b in g], [b.ptr for b in out])
+            keep += g
+            packed.append(out)
+        red = [DevBuf(W * S * ESZ[r], off(r)) for r, S in zip(rho, pl.bucket_S)]
+        fp.fsdp_emulated_reduce_scatter(L, [packed[q][b].ptr for b in range(len(rho)) for q in range(W)],
+                                        [b.ptr for b in red])
+        fp.fsdp_sync_status(L)
+        want_red = oracle.emulated_reduce_scatter(pl, [oracle.pack_reduce_scatter(pl, grads[q]) for q in range(W)])
+        for b, (buf, r, want) in enumerate(zip(red, rho, want_red)):
+            got = buf.read(NP[r])
+            assert np.array_equal(got, want), f"emulated reduce-scatter, bucket {b}: {first_mismatch(got, want)}"
+            assert buf.guards_ok()
+        for r in range(W):
+            sharded = [DevBuf(c * ESZ[s.shard_dtype], 0) for s, c in zip(specs, pl.chunk)]
+            fp.fsdp_reduce_scatter_copy_out(L, [buf.ptr + r * S * ESZ[rr] for buf, S, rr in zip(red, pl.bucket_S, rho)],
+                                            [b.ptr for b in sharded])
+            fp.fsdp_sync_status(L)
+            rows = [w[r * S:(r + 1) * S] for w, S in zip(want_red, pl.bucket_S)]
+            for p, (buf, s, want) in enumerate(zip(sharded, specs, oracle.reduce_scatter_copy_out(pl, rows))):
+                got = buf.read(NP[s.shard_dtype])
+                assert np.array_equal(got, want), f"rank {r} sharded grad {p}: {first_mismatch(got, want)}"
+
+
+@pytest.mark.parametrize("same_phase", [True, False])
+def test_end_to_end_pack_emulated_reduce_scatter_copy_out(fp, same_phase):
+    for seed in range(40):
+        work = wl.random_layout(8000 + seed, max_params=5, max_numel=3000, W_choices=(1, 2, 3, 4, 8))
+        _end_to_end(fp, work.groups[0], work.W, work, seed, same_phase)
+    work = wl.transformer_500(W=8, layers=1)
+    _end_to_end(fp, work.groups[0], 8, work, 99, same_phase)
+    work = wl.kda_block(W=8, reduce="grad", d=512, ffn=1536)
+    _end_to_end(fp, work.groups[0], 8, work, 98, same_phase)
+
+
 def test_batched_transformer500_all_layers_in_one_launch(fp):
     work = wl.transformer_500(W=8)
     runs = [GroupRun(fp, specs, work.W, work, g) for g, specs in enumerate(work.groups)]
