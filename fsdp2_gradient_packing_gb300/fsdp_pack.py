@@ -282,47 +282,51 @@ def fsdp_emulated_reduce_scatter(layout: Layout, packed, reduced, stream=None) -
                                              _stream(stream)), "fsdp_emulated_reduce_scatter")
 
 
-def layout_array(layouts):
-    """A C array of layout handles; pass it in place of a list to skip
-    re-marshalling on every call."""
-    if isinstance(layouts, ctypes.Array):
-        return layouts
-    arr = (_LAYOUT * max(1, len(layouts)))()
-    for k, L in enumerate(layouts):
-        arr[k] = L.handle
-    return arr
+class LayoutArray:
+    """A C array of layout handles plus its length; pass it in place of a
+    list of layouts to skip re-marshalling on every batched call."""
+
+    def __init__(self, layouts):
+        self.n = len(layouts)
+        self.arr = (_LAYOUT * max(1, self.n))()
+        for k, L in enumerate(layouts):
+            self.arr[k] = L.handle
+
+
+def layout_array(layouts) -> LayoutArray:
+    return layouts if isinstance(layouts, LayoutArray) else LayoutArray(layouts)
 
 
 def fsdp_pack_reduce_scatter_batched(layouts, grads, bucket_bufs, stream=None) -> None:
     """grads / bucket_bufs: the per-layout lists concatenated in layout order."""
-    arr = layout_array(layouts)
-    _check(_lib.fsdp_pack_reduce_scatter_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
-                                                 pointer_array(grads), pointer_array(bucket_bufs), _stream(stream)),
+    la = layout_array(layouts)
+    _check(_lib.fsdp_pack_reduce_scatter_batched(la.arr, la.n, pointer_array(grads), pointer_array(bucket_bufs),
+                                                 _stream(stream)),
            "fsdp_pack_reduce_scatter_batched")
 
 
 def fsdp_allgather_copy_in_batched(layouts, local_shards, ag_inputs, stream=None) -> None:
     """local_shards concatenated in layout order; one ag_input per layout."""
-    arr = layout_array(layouts)
-    _check(_lib.fsdp_allgather_copy_in_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
-                                               pointer_array(local_shards), pointer_array(ag_inputs), _stream(stream)),
+    la = layout_array(layouts)
+    _check(_lib.fsdp_allgather_copy_in_batched(la.arr, la.n, pointer_array(local_shards), pointer_array(ag_inputs),
+                                               _stream(stream)),
            "fsdp_allgather_copy_in_batched")
 
 
 def fsdp_allgather_copy_out_batched(layouts, ag_outputs, full_params, stream=None) -> None:
     """One ag_output per layout; full_params concatenated in layout order."""
-    arr = layout_array(layouts)
-    _check(_lib.fsdp_allgather_copy_out_batched(arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts),
-                                                pointer_array(ag_outputs), pointer_array(full_params), _stream(stream)),
+    la = layout_array(layouts)
+    _check(_lib.fsdp_allgather_copy_out_batched(la.arr, la.n, pointer_array(ag_outputs), pointer_array(full_params),
+                                                _stream(stream)),
            "fsdp_allgather_copy_out_batched")
 
 
 def fsdp_reduce_scatter_copy_out_batched(layouts, reduced_rows, sharded_grads, stream=None) -> None:
     """reduced_rows / sharded_grads: the per-layout lists concatenated in layout order."""
-    arr = layout_array(layouts)
-    _check(_lib.fsdp_reduce_scatter_copy_out_batched(
-        arr, len(arr) if isinstance(layouts, ctypes.Array) else len(layouts), pointer_array(reduced_rows),
-        pointer_array(sharded_grads), _stream(stream)), "fsdp_reduce_scatter_copy_out_batched")
+    la = layout_array(layouts)
+    _check(_lib.fsdp_reduce_scatter_copy_out_batched(la.arr, la.n, pointer_array(reduced_rows),
+                                                     pointer_array(sharded_grads), _stream(stream)),
+           "fsdp_reduce_scatter_copy_out_batched")
 
 
 def fsdp_pack_reduce_scatter_noalloc(layout: Layout, grads, bucket_bufs, stream=None) -> None:

@@ -245,6 +245,49 @@ def test_batched_with_empty_layouts(fp):
             run.close()
 
 
+def test_many_ranks_and_ranks_past_the_end(fp):
+    # W far above the parameters' sizes: most ranks hold pure padding.
+    specs = (wl.ParamSpec("a", (5,), "bf16"), wl.ParamSpec("b", (3, 7), "f32", "bf16"), wl.ParamSpec("c", (1,)))
+    for W in (9, 100, 1000):
+        work = wl.Workload(f"wide{W}", W, (specs,), seed=W)
+        assert_group_parity(fp, specs, W, work, 0, misalign_seed=W, specials=0.1)
+        assert_group_parity(fp, specs, W, work, 0, misalign_seed=W + 1, specials=0.1, rows=True)
+
+
+def test_one_layout_from_several_host_threads(fp):
+    """A layout is only read after planning: threads may share it, each on
+    its own stream."""
+    import threading
+    work = wl.transformer_500(W=8, layers=1)
+    specs = work.groups[0]
+    run = GroupRun(fp, specs, 8, work, 0)
+    want = run.pack_expected()[0]
+    grads = [DevBuf(g.nbytes, 0, g) for g in run.grads]
+    outs = [DevBuf(8 * run.pl.bucket_S[0] * 4) for _ in range(6)]
+    errors = []
+
+    def worker(k):
+        try:
+            s = torch.cuda.Stream()
+            for _ in range(20):
+                fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [outs[k].ptr], s)
+            s.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+    try:
+        threads = [threading.Thread(target=worker, args=(k,)) for k in range(6)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        assert not errors, errors
+        fp.fsdp_sync_status(run.L)
+        for o in outs:
+            assert np.array_equal(o.read(np.uint32), want)
+    finally:
+        run.close()
+
+
 def test_empty_layout_and_empty_parameters(fp):
     with fp.fsdp_plan_layout([], 8) as L:
         fp.fsdp_pack_reduce_scatter(L, [], [])
