@@ -164,11 +164,17 @@ def read_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel and planner sources with comments and whitespace
+    removed, so that only a change of code invalidates a profile."""
+    import re
     h = hashlib.sha256()
     for rel in ("fsdp2_gradient_packing_gb300/csrc/kernels.cu", "fsdp2_gradient_packing_gb300/csrc/layout.h",
                 "fsdp2_gradient_packing_gb300/csrc/plan.cpp"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,10 +1,15 @@
 // sm_103a kernels and the launching entry points of the C ABI.
 //
-// All three operations (reduce-scatter copy-in, all-gather copy-in, all-gather
-// copy-out) are "walk a table of contiguous runs and copy each one with a
-// cast": dst[k] = k < n_copy ? cast(src[k]) : +0 for k < n_total.  The host
-// planner (plan.cpp) emits the runs once per layout, cut into work items of at
-// most kStageBytes of source; one launch per call walks them.
+// The four packing operations (reduce-scatter copy-in, all-gather copy-in,
+// all-gather copy-out, reduce-scatter copy-out) are all "walk a table of
+// contiguous runs and copy each one with a cast": dst[k] = k < n_copy ?
+// cast(src[k]) : +0 for k < n_total.  The host planner (plan.cpp) emits the
+// runs once per layout, cut into work items of at most kStageBytes of source;
+// one launch per call walks them (walk_kernel), or, for the *_batched calls,
+// one launch walks the tables of up to 64 layouts.  Every launch uses
+// programmatic dependent launch: it may be scheduled while the previous kernel
+// on the stream drains, and waits for it before touching memory.  A separate
+// elementwise kernel (sum_kernel) serves the emulated reduce-scatter.
 //
 // The work is bound by HBM bandwidth, so the kernel is a warp-specialised
 // pipeline built to keep many bytes in flight per SM with few registers and
