@@ -288,6 +288,56 @@ def test_one_layout_from_several_host_threads(fp):
         run.close()
 
 
+def test_calls_replay_from_a_cuda_graph(fp):
+    """The entry points only launch kernels (planning and its allocation come
+    first), so a step can be captured in a CUDA graph and replayed."""
+    work = wl.transformer_500(W=4, layers=1)
+    specs = work.groups[0]
+    run = GroupRun(fp, specs, 4, work, 0, specials=0.02)
+    try:
+        pl = run.pl
+        grads = [DevBuf(g.nbytes, 0, g) for g in run.grads]
+        bucket = DevBuf(4 * pl.bucket_S[0] * 4)
+        shards = [[DevBuf(x.nbytes, 0, x) for x in row] for row in run.shards]
+        gathered = DevBuf(4 * pl.S_ag)
+        full = [DevBuf(s.numel * ESZ[s.param_dtype]) for s in specs]
+        rows = [DevBuf(x.nbytes, 0, x) for x in run.rows]
+        sharded = [DevBuf(c * ESZ[s.shard_dtype]) for s, c in zip(specs, pl.chunk)]
+
+        def step():
+            fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [bucket.ptr])
+            for r in range(4):
+                fp.fsdp_allgather_copy_in(run.L, [b.ptr for b in shards[r]], gathered.ptr + r * pl.S_ag)
+            fp.fsdp_allgather_copy_out(run.L, gathered.ptr, [b.ptr for b in full])
+            fp.fsdp_reduce_scatter_copy_out(run.L, [b.ptr for b in rows], [b.ptr for b in sharded])
+
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()                                   # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for buf in [bucket, gathered] + full + sharded:
+            buf.raw[buf.off:buf.off + buf.nbytes].fill_(0x5A)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        fp.fsdp_sync_status(run.L)
+        assert np.array_equal(bucket.read(np.uint32), run.pack_expected()[0])
+        want_rows, want_full = run.gather_expected()
+        assert np.array_equal(gathered.read(), want_rows)
+        for b, s_, w in zip(full, specs, want_full):
+            assert np.array_equal(b.read(NP[s_.param_dtype]), w)
+        for b, s_, w in zip(sharded, specs, run.rs_copy_out_expected()):
+            assert np.array_equal(b.read(NP[s_.shard_dtype]), w)
+    finally:
+        run.close()
+
+
 def test_empty_layout_and_empty_parameters(fp):
     with fp.fsdp_plan_layout([], 8) as L:
         fp.fsdp_pack_reduce_scatter(L, [], [])
