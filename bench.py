@@ -69,6 +69,13 @@ WORKLOADS = {
     "transformer500": (lambda: wl.transformer_500(W=8),
                        "transformer500_W8: 24 fully_shard groups (one per layer, d=512, 17 tensors each, "
                        "408 in all), W=8, reduce FP32, shards FP32, params BF16 matrices / FP32 small"),
+    "transformer500_homogeneous": (lambda: wl.transformer_500(W=8, homogeneous=True),
+                                   "transformer500_W8 with param dtype BF16 for every parameter (one all-gather "
+                                   "dtype group): the homogeneous counterpart of transformer500"),
+    "kda8": (lambda: wl.kda_block(W=8, reduce="f32", blocks=8),
+             "kda8_W8: all 8 KDA-style blocks (1,744,929,024 parameters), one fully_shard group per block, W=8"),
+    "kda8_homogeneous": (lambda: wl.kda_block(W=8, reduce="f32", blocks=8, homogeneous=True),
+                         "kda8_W8 with param dtype BF16 for every parameter: the homogeneous counterpart of kda8"),
     "kda_w8": (lambda: wl.kda_block(W=8, reduce="f32"),
                "kda_block_W8: one KDA-style block at d=4096 (218,116,128 parameters), W=8, reduce FP32"),
     "kda_w64": (lambda: wl.kda_block(W=64, reduce="f32"),
@@ -89,7 +96,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=30,
+                    help="timed end-to-end steps (0: skip the end-to-end pass, e.g. for layouts too large to "
+                         "stage in pinned host memory twice)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed50m",
                     help="layout to time (the benchmark's metric is quoted on mixed50m)")
     ap.add_argument("--rs-copy-out", action="store_true",
@@ -567,6 +576,27 @@ def run_ours(args):
         fp.fsdp_sync_status(grp.L)
     per = {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs] for j, k in enumerate(OPS)}
 
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, fp, torch, groups, h, rs, step_bytes, world)
+
+    result = None
+    if rank == 0:
+        result = report(args, work, description, groups, nbytes, step_bytes, total_ms, per, clocks, e2e,
+                        n_launch, rs, world, K)
+    for grp in groups:
+        grp.L.close()
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        samp = OracleSampler(work, inputs)
+        result["cpu_baseline"] = cpu_baseline(samp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
+def run_e2e(args, fp, torch, groups, h, rs, step_bytes, world):
     # End to end through the same API with host buffers: every step copies
     # its inputs from pinned host memory and reads its results back.  Steps
     # are pipelined the way a caller would run them: uploads on one stream,
@@ -637,60 +667,54 @@ def run_ours(args):
     for grp in groups:
         fp.fsdp_sync_status(grp.L)
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device=torch.device("cuda"))
+    return {"value": world * step_bytes * E / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+            "note": "host buffers; uploads, kernels and downloads of consecutive steps pipelined "
+                    "on three streams with two buffer sets"}
 
-    result = None
-    if rank == 0:
-        peak, peak_kind = read_peaks()
-        pack_ms = statistics.mean(per["pack"])
-        achieved = nbytes["pack"] / (pack_ms * 1e-3) / 1e9
-        rows = {k: {"bytes": nbytes[k], "launches_per_step": n_launch, "ms_mean": statistics.mean(v),
-                    "ms_median": statistics.median(v), "ms_min": min(v),
-                    "gbs": nbytes[k] / (statistics.mean(v) * 1e-3) / 1e9}
-                for k, v in per.items()}
-        result = {
-            "metric": METRIC,
-            "value": world * step_bytes * K / (total_ms * 1e-3) / 1e9,
-            "unit": UNIT,
-            "n_gpus": world,
-            "steps": K,
-            "warmup": args.warmup,
-            "ms_per_step": total_ms / K,
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "bf16+f32",
-            "data": "synthetic",
-            "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else "")
-                       + (STEP_ERS if args.emulated_rs else ""), "world_size_layout": work.W,
-                       "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
-                       "parallelism": f"replicas x{world} (no data-path collective)",
-                       "l2": "inputs larger than L2: two rotating buffer sets of "
-                             f"{2 * step_bytes / 1e9:.2f} GB of algorithmic traffic vs 129 MB L2; no flush"},
-            "ops": rows,
-            "ops_note": "per-operation device times from a second pass of the same K steps with CUDA "
-                        "events around every launch (summed over the step's groups)",
-            "roofline": {"bound": "hbm", "kernel": "walk_kernel (reduce-scatter pack launches)",
-                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "peak_source": f"{peak_kind} hbm_gbs (burst copy)" if peak_kind == "measured" else "fallback",
-                         "bytes_per_launch": nbytes["pack"] / n_launch,
-                         "traffic": read_traffic() if args.workload == "mixed50m" else None},
-            "e2e": {"value": world * step_bytes * E / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
-                    "note": "host buffers; uploads, kernels and downloads of consecutive steps pipelined "
-                            "on three streams with two buffer sets"},
-            "gpu_launches": len(OPS) * n_launch * K,
-            "clocks": clocks,
-        }
-    for grp in groups:
-        grp.L.close()
-    if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        samp = OracleSampler(work, inputs)
-        result["cpu_baseline"] = cpu_baseline(samp, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(result), flush=True)
-    import torch.distributed as dist
-    if dist.is_initialized():
-        dist.destroy_process_group()
+
+def report(args, work, description, groups, nbytes, step_bytes, total_ms, per, clocks, e2e, n_launch, rs,
+           world, K):
+    """The JSON result of our arm (rank 0)."""
+    peak, peak_kind = read_peaks()
+    pack_ms = statistics.mean(per["pack"])
+    achieved = nbytes["pack"] / (pack_ms * 1e-3) / 1e9
+    rows = {k: {"bytes": nbytes[k], "launches_per_step": n_launch, "ms_mean": statistics.mean(v),
+                "ms_median": statistics.median(v), "ms_min": min(v),
+                "gbs": nbytes[k] / (statistics.mean(v) * 1e-3) / 1e9}
+            for k, v in per.items()}
+    result = {
+        "metric": METRIC,
+        "value": world * step_bytes * K / (total_ms * 1e-3) / 1e9,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16+f32",
+        "data": "synthetic",
+        "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else "")
+                   + (STEP_ERS if args.emulated_rs else ""), "world_size_layout": work.W,
+                   "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
+                   "parallelism": f"replicas x{world} (no data-path collective)",
+                   "l2": "inputs larger than L2: two rotating buffer sets of "
+                         f"{2 * step_bytes / 1e9:.2f} GB of algorithmic traffic vs 129 MB L2; no flush"},
+        "ops": rows,
+        "ops_note": "per-operation device times from a second pass of the same K steps with CUDA "
+                    "events around every launch (summed over the step's groups)",
+        "roofline": {"bound": "hbm", "kernel": "walk_kernel (reduce-scatter pack launches)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)" if peak_kind == "measured" else "fallback",
+                     "bytes_per_launch": nbytes["pack"] / n_launch,
+                     "traffic": read_traffic() if args.workload == "mixed50m" else None},
+        "e2e": e2e,
+        "gpu_launches": len(per) * n_launch * K,
+        "clocks": clocks,
+    }
+    return result
 
 
 # ---------------------------------------------------------------------------

@@ -85,14 +85,15 @@ def tiny_two_blocks(W: int = 4, grouping: str = "linear") -> Workload:
     return Workload(f"tiny_two_blocks_{grouping}", W, groups, std=1.0, seed=1000)
 
 
-def transformer_500(W: int = 8, layers: int = 24) -> Workload:
+def transformer_500(W: int = 8, layers: int = 24, homogeneous: bool = False) -> Workload:
     """~500-parameter transformer-like layout, one fully_shard group per layer.
 
     Each layer: attn_norm[512] FP32, q/k/v/o [512, 512] BF16, mlp_norm[512]
     FP32, gate/up [1408, 512] BF16, down [512, 1408] BF16, and eight FP32
     scalar/vector parameters s0..s7 whose lengths are drawn from U{1..64}.
     Gradients are in the parameter's own dtype; reduce dtype FP32; local
-    shards FP32; param dtype BF16 for the matrices and FP32 for the rest.
+    shards FP32; param dtype BF16 for the matrices and FP32 for the rest
+    (``homogeneous``: BF16 for every parameter, one all-gather dtype group).
     """
     rnd = random.Random(2001)
     groups = []
@@ -106,8 +107,11 @@ def transformer_500(W: int = 8, layers: int = 24) -> Workload:
         g.append(ParamSpec(f"l{layer}.down", (512, 1408), "bf16", "f32", "f32", "bf16"))
         for s in range(8):
             g.append(ParamSpec(f"l{layer}.s{s}", (rnd.randint(1, 64),), "f32", "f32", "f32", "f32"))
+        if homogeneous:
+            g = [ParamSpec(p.name, p.shape, p.grad_dtype, p.reduce_dtype, p.shard_dtype, "bf16") for p in g]
         groups.append(tuple(g))
-    return Workload(f"transformer500_W{W}", W, tuple(groups), std=0.02, seed=1001)
+    return Workload(f"transformer500_W{W}" + ("_homogeneous" if homogeneous else ""), W, tuple(groups),
+                    std=0.02, seed=1001)
 
 
 def mixed_50m(W: int = 8, layers: int = 4) -> Workload:
@@ -130,7 +134,7 @@ def mixed_50m(W: int = 8, layers: int = 4) -> Workload:
 
 
 def kda_block(W: int = 8, reduce: str = "f32", blocks: int = 1, d: int = 4096,
-              heads: int = 32, ffn: int = 12288) -> Workload:
+              heads: int = 32, ffn: int = 12288, homogeneous: bool = False) -> Workload:
     """KDA-style transformer blocks, one fully_shard group per block.
 
     Per block: attn_norm[d] FP32, q/k/v/o [d, d] BF16, decay[heads] FP32,
@@ -138,7 +142,8 @@ def kda_block(W: int = 8, reduce: str = "f32", blocks: int = 1, d: int = 4096,
     w_down [d, ffn] BF16.  Eight blocks at d=4096 hold 1,744,929,024
     parameters.  ``reduce``: "f32" puts everything in one FP32 bucket, "grad"
     gives each parameter the reduce dtype of its gradient (a BF16 and an FP32
-    bucket), "bf16" reduces everything in BF16.
+    bucket), "bf16" reduces everything in BF16.  Param dtype: BF16 for the
+    matrices, FP32 for the small parameters (``homogeneous``: BF16 for all).
     """
     groups = []
     for blk in range(blocks):
@@ -146,7 +151,7 @@ def kda_block(W: int = 8, reduce: str = "f32", blocks: int = 1, d: int = 4096,
 
         def add(name, shape, dt):
             rd = {"f32": "f32", "bf16": "bf16", "grad": dt}[reduce]
-            pd = "bf16" if dt == "bf16" else "f32"
+            pd = "bf16" if (dt == "bf16" or homogeneous) else "f32"
             g.append(ParamSpec(f"b{blk}.{name}", shape, dt, rd, "f32", pd))
 
         add("attn_norm", (d,), "f32")
@@ -159,7 +164,8 @@ def kda_block(W: int = 8, reduce: str = "f32", blocks: int = 1, d: int = 4096,
         add("w_up", (ffn, d), "bf16")
         add("w_down", (d, ffn), "bf16")
         groups.append(tuple(g))
-    return Workload(f"kda_W{W}_reduce-{reduce}", W, tuple(groups), std=1.0, seed=1004)
+    return Workload(f"kda_W{W}_reduce-{reduce}" + ("_homogeneous" if homogeneous else ""), W, tuple(groups),
+                    std=1.0, seed=1004)
 
 
 # ---------------------------------------------------------------------------
