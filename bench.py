@@ -56,6 +56,7 @@ from fsdp2_gradient_packing_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "reduce-scatter pack GB/s and ms per fully_shard (50.3M elem, W=8) vs HBM peak"
 UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the metric is quoted against
 FALLBACK_HBM_GBS = 6800.0
 ESZ = {"f32": 4, "bf16": 2}
 STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
@@ -105,6 +106,10 @@ def parse_args(argv=None):
                     help="add the reduce-scatter copy-out (reduced rows to sharded gradients) to every step")
     ap.add_argument("--emulated-rs", action="store_true",
                     help="add the emulated reduce-scatter (sum of W ranks' packed buffers) after the pack")
+    ap.add_argument("--precast-iters", type=int, default=200,
+                    help="iterations of the pre-cast-then-pack comparison (0 = skip)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as replays of a CUDA graph holding two steps (both buffer sets)")
     ap.add_argument("--batched", action="store_true",
                     help="one launch per operation for all of the workload's groups (*_batched entry points)")
     return ap.parse_args(argv)
@@ -503,6 +508,71 @@ class Batch:
                 ev[4].record()
 
 
+def precast_comparison(fp, torch, work, grp, h, iters):
+    """The sequence the fused pack replaces: every BF16 gradient that reduces in
+    FP32 is first cast into one FP32 temporary, then an FP32 -> FP32 pack reads
+    the temporary ("FSDP2 per-parameter mixed precision", results table:
+    copy-in with the cast fused against a separate pre-cast).  Both steps run
+    on this library's own kernel: the cast is a pack on a one-rank layout (one
+    bucket, c_p = n_p, no padding: a plain cast and concatenation).  The
+    temporary is allocated once, as a caching allocator would hand it back.
+    Timed as a loop of (cast, pack) pairs beside a loop of the fused pack alone,
+    both alternating the two buffer sets, CUDA events on the launching stream."""
+    import dataclasses
+    specs = grp.specs
+    cast_idx = [i for i, s in enumerate(specs) if s.grad_dtype == "bf16" and s.reduce_dtype == "f32"]
+    if not cast_idx or iters <= 0:
+        return None
+    cast_specs = [dataclasses.replace(specs[i], reduce_dtype="f32") for i in cast_idx]
+    fp32_specs = [dataclasses.replace(s, grad_dtype="f32") if i in set(cast_idx) else s
+                  for i, s in enumerate(specs)]
+    with fp.fsdp_plan_layout(cast_specs, 1) as L_cast, fp.fsdp_plan_layout(fp32_specs, work.W) as L32:
+        tmp_bytes = fp.fsdp_layout_bucket(L_cast, 0).bytes
+        tmp = torch.empty(tmp_bytes, dtype=torch.uint8, device="cuda")
+        offs = {i: fp.fsdp_layout_param(L_cast, k).bucket_offset * 4 for k, i in enumerate(cast_idx)}
+        args = []
+        for st in grp.sets:
+            cast_src = fp.pointer_array([st.grad_ptrs[i] for i in cast_idx])
+            tmp_dst = fp.pointer_array([tmp.data_ptr()])
+            grads32 = fp.pointer_array([tmp.data_ptr() + offs[i] if i in offs else st.grad_ptrs[i]
+                                        for i in range(len(specs))])
+            args.append((cast_src, tmp_dst, grads32, st.bucket_ptrs, st.grad_ptrs))
+
+        def precast(k):
+            a = args[k & 1]
+            fp.fsdp_pack_reduce_scatter(L_cast, a[0], a[1], h)
+            fp.fsdp_pack_reduce_scatter(L32, a[2], a[3], h)
+
+        def fused(k):
+            a = args[k & 1]
+            fp.fsdp_pack_reduce_scatter(grp.L, a[4], a[3], h)
+
+        def loop(fn):
+            for k in range(10):
+                fn(k)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for k in range(iters):
+                fn(k)
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / iters
+
+        pre_ms, fused_ms = loop(precast), loop(fused)
+        for L in (L_cast, L32, grp.L):
+            fp.fsdp_sync_status(L)
+        bucket_bytes = [fp.fsdp_layout_bucket(L32, b).bytes for b in range(fp.fsdp_layout_query(L32).n_buckets)]
+        pre_bytes = (op_bytes(cast_specs, 1, [tmp_bytes], 0)["pack"]
+                     + op_bytes(fp32_specs, work.W, bucket_bytes, 0)["pack"])
+        del tmp
+    return {"what": "BF16 gradients cast into one FP32 temporary, then the FP32 -> FP32 pack, "
+                    "against the fused pack; back-to-back loops of " + str(iters),
+            "temporary_bytes": tmp_bytes, "precast_ms": pre_ms, "fused_ms": fused_ms,
+            "precast_over_fused": pre_ms / fused_ms, "precast_bytes": pre_bytes,
+            "precast_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9, "launches": 2 * iters + iters}
+
+
 def run_steps(fp, groups, h, first, count, evs=None, batch=None, rs=False):
     for i in range(first, first + count):
         if batch is not None:
@@ -540,6 +610,20 @@ def run_ours(args):
         fp.fsdp_sync_status(grp.L)
 
     K = args.steps
+    graph = None
+    if args.graph:
+        # Two steps (buffer sets 0 and 1) captured once and replayed K / 2
+        # times: the layers' launches go to the GPU without host involvement.
+        K += K & 1
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            run_steps(fp, groups, torch.cuda.current_stream().cuda_stream, 0, 2, batch=batch, rs=rs)
+        for _ in range(max(1, args.warmup // 2)):
+            graph.replay()
+        torch.cuda.synchronize()
+        for grp in groups:
+            fp.fsdp_sync_status(grp.L)
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -554,7 +638,11 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first sample before the load starts
     t_start.record()
-    run_steps(fp, groups, h, 0, K, batch=batch, rs=rs)
+    if graph is not None:
+        for _ in range(K // 2):
+            graph.replay()
+    else:
+        run_steps(fp, groups, h, 0, K, batch=batch, rs=rs)
     t_end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -576,6 +664,10 @@ def run_ours(args):
         fp.fsdp_sync_status(grp.L)
     per = {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs] for j, k in enumerate(OPS)}
 
+    precast = None
+    if len(groups) == 1 and args.precast_iters > 0:
+        precast = precast_comparison(fp, torch, work, groups[0], h, args.precast_iters)
+
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(args, fp, torch, groups, h, rs, step_bytes, world)
@@ -584,6 +676,8 @@ def run_ours(args):
     if rank == 0:
         result = report(args, work, description, groups, nbytes, step_bytes, total_ms, per, clocks, e2e,
                         n_launch, rs, world, K)
+        if precast is not None:
+            result["precast_baseline"] = precast
     for grp in groups:
         grp.L.close()
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -699,6 +793,8 @@ def report(args, work, description, groups, nbytes, step_bytes, total_ms, per, c
         "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else "")
                    + (STEP_ERS if args.emulated_rs else ""), "world_size_layout": work.W,
                    "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
+                   "launch": ("CUDA graph of two steps, replayed" if args.graph
+                              else "stream launches from the host") + (", batched over groups" if args.batched else ""),
                    "parallelism": f"replicas x{world} (no data-path collective)",
                    "l2": "inputs larger than L2: two rotating buffer sets of "
                          f"{2 * step_bytes / 1e9:.2f} GB of algorithmic traffic vs 129 MB L2; no flush"},
@@ -707,6 +803,7 @@ def report(args, work, description, groups, nbytes, step_bytes, total_ms, per, c
                     "events around every launch (summed over the step's groups)",
         "roofline": {"bound": "hbm", "kernel": "walk_kernel (reduce-scatter pack launches)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)" if peak_kind == "measured" else "fallback",
                      "bytes_per_launch": nbytes["pack"] / n_launch,
                      "traffic": read_traffic() if args.workload == "mixed50m" else None},
