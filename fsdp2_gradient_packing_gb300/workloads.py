@@ -186,6 +186,20 @@ def normal_bits(n: int, dtype: str, std: float, seed: int, *key: int) -> np.ndar
     return (bits >> np.uint32(16)).astype(np.uint16)
 
 
+def device_random_bytes(nbytes: int, seed: int, *key: int):
+    """``nbytes`` uniformly random bytes on the current CUDA device, drawn by
+    torch's seeded Philox generator: read as FP32 or BF16 elements, every bit
+    pattern is equally likely (NaNs, infinities and subnormals included) and
+    the values never repeat with a period that an offset error could hide
+    behind.  For inputs of billions of elements, where host generation would
+    take minutes; copy the tensor to the host for the oracle."""
+    import torch
+    state = np.random.SeedSequence([seed, *key]).generate_state(1, np.uint64)[0]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(int(state))
+    return torch.randint(0, 256, (int(nbytes),), dtype=torch.uint8, device="cuda", generator=g)
+
+
 # Special FP32 bit patterns: signed zeros, infinities, NaNs with payloads,
 # subnormals, extremes, and values whose low 16 bits sit exactly on, just
 # below and just above a BF16 rounding tie.
