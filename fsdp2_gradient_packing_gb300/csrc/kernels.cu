@@ -596,13 +596,25 @@ __device__ __forceinline__ uint32_t add_bits(uint32_t acc, uint32_t x) {
   }
 }
 
+// Two BF16 sums at once: the two binary32 additions, then one hardware
+// round-to-nearest-even conversion of both sums to a BF16 pair (the same
+// rounding add_bits does with integer operations, in one instruction), then
+// a NaN sum in either half becomes the canonical quiet NaN.
+__device__ __forceinline__ uint32_t add_bf16_pair(uint32_t x, uint32_t y) {
+  const float s_lo = __fadd_rn(__uint_as_float(x << 16), __uint_as_float(y << 16));
+  const float s_hi = __fadd_rn(__uint_as_float(x & 0xFFFF0000u), __uint_as_float(y & 0xFFFF0000u));
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(s_hi), "f"(s_lo));
+  if (s_lo != s_lo) d = (d & 0xFFFF0000u) | 0x7FC0u;
+  if (s_hi != s_hi) d = (d & 0x0000FFFFu) | 0x7FC00000u;
+  return d;
+}
+
 // Lane-wise sum of two 16-byte vectors of elements.
 template <bool BF16>
 __device__ __forceinline__ uint4 add_vec(uint4 a, uint4 b) {
   if constexpr (BF16) {
-    auto pair = [](uint32_t x, uint32_t y) {
-      return add_bits<true>(x & 0xFFFFu, y & 0xFFFFu) | (add_bits<true>(x >> 16, y >> 16) << 16);
-    };
+    auto pair = [](uint32_t x, uint32_t y) { return add_bf16_pair(x, y); };
     return make_uint4(pair(a.x, b.x), pair(a.y, b.y), pair(a.z, b.z), pair(a.w, b.w));
   } else {
     return make_uint4(add_bits<false>(a.x, b.x), add_bits<false>(a.y, b.y), add_bits<false>(a.z, b.z),

@@ -207,6 +207,42 @@ def test_end_to_end_pack_emulated_reduce_scatter_copy_out(fp, same_phase):
     _end_to_end(fp, work.groups[0], 8, work, 98, same_phase)
 
 
+# BF16 partners for the rounding sweep below: signed zeros, subnormals, the
+# smallest normal, values that put the FP32 sum exactly on, just below and just
+# above a BF16 rounding tie (2**-8, 2**-9, 1.5 * 2**-8, 2**-16 against 1.0 and
+# its neighbours), the largest finite values (sums that overflow to infinity),
+# infinities (inf - inf) and NaNs with payloads.
+BF16_PARTNERS = [0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080,
+                 0x3F80, 0xBF80, 0x3B80, 0xBB80, 0x3B00, 0x3BC0, 0x3780, 0x37C0, 0x3B40,
+                 0x7F7F, 0xFF7F, 0x7F00, 0x7EFF, 0x4000, 0xC000, 0x7F80, 0xFF80,
+                 0x7FC0, 0xFFC1, 0x7F81, 0x4B00, 0x3400]
+
+
+@pytest.mark.parametrize("phase", [0, 2])
+def test_emulated_rs_bf16_rounding_on_every_first_operand(fp, phase):
+    """Two-rank BF16 sums of every one of the 65,536 BF16 patterns with each
+    partner (plus seeded random partners): every pair's FP32 sum rounded to
+    BF16 bit for bit against the oracle, through the vector path (equal phases)
+    and the element path (phase 2 on one input)."""
+    partners = np.array(BF16_PARTNERS + list(wl.normal_bits(34, "bf16", 1.0, 7100, 0)), np.uint16)
+    K = partners.size
+    n = K * 65536
+    specs = [wl.ParamSpec("p", (n,), "bf16", "bf16", "f32", "bf16")]
+    pl = oracle.plan(oracle.params_from_specs(specs), 2)
+    assert 2 * pl.bucket_S[0] == n
+    a = np.tile(np.arange(65536, dtype=np.uint32).astype(np.uint16), K)
+    b = np.repeat(partners, 65536)
+    want, = oracle.emulated_reduce_scatter(pl, [[a], [b]])
+    with fp.fsdp_plan_layout(specs, 2) as L:
+        ins = [DevBuf(2 * n, 0, a), DevBuf(2 * n, phase, b)]
+        out = DevBuf(2 * n)
+        fp.fsdp_emulated_reduce_scatter(L, [x.ptr for x in ins], [out.ptr])
+        fp.fsdp_sync_status(L)
+        got = out.read(np.uint16)
+    assert out.guards_ok()
+    assert np.array_equal(got, want), first_mismatch(got, want)
+
+
 def test_batched_transformer500_all_layers_in_one_launch(fp):
     work = wl.transformer_500(W=8)
     runs = [GroupRun(fp, specs, work.W, work, g) for g, specs in enumerate(work.groups)]
