@@ -3,8 +3,10 @@
 Each function here has the name of the C entry point it calls and only
 marshals arguments: tensors become device pointers (``data_ptr()``), the
 stream becomes a ``cudaStream_t`` handle, and a non-OK status becomes an
-``FsdpError``.  All packing work runs in the library's CUDA kernels; there is
-no fallback path.  Importing this module fails if the library has not been
+``FsdpError``.  Because the C functions read as many pointers as the layout
+has slots, the binding first checks the pointer counts, and the size, dtype,
+contiguity and device of any torch tensor it is given (``ValueError``).  All
+packing work runs in the library's CUDA kernels; there is no fallback path.  Importing this module fails if the library has not been
 built (``__graft_entry__.build()`` or ``python -m
 fsdp2_gradient_packing_gb300._build``).
 """
@@ -126,11 +128,16 @@ def fsdp_last_error() -> str:
 
 
 class Layout:
-    """Owner of an ``fsdp_layout_t *``; destroyed on ``close()`` or collection."""
+    """Owner of an ``fsdp_layout_t *``; destroyed on ``close()`` or collection.
+    Keeps the parameter descriptors it was planned from, so that the entry
+    points can check the buffers they are given against it."""
 
-    def __init__(self, handle: int, n_params: int):
+    def __init__(self, handle: int, n_params: int, descs=None):
         self.handle = handle
         self.n_params = n_params
+        self.descs = [(d.numel, d.grad_dtype, d.reduce_dtype, d.shard_dtype, d.param_dtype)
+                      for d in (descs or [])][:n_params]
+        self._slots = None
 
     def close(self) -> None:
         if self.handle:
@@ -169,7 +176,7 @@ def fsdp_plan_layout(params, world_size: int) -> Layout:
     arr = _descs(params)
     out = _LAYOUT()
     _check(_lib.fsdp_plan_layout(arr, len(params), world_size, ctypes.byref(out)), "fsdp_plan_layout")
-    return Layout(out.value, len(params))
+    return Layout(out.value, len(params), arr)
 
 
 def fsdp_plan_layout_host(params, world_size: int) -> Layout:
@@ -177,7 +184,7 @@ def fsdp_plan_layout_host(params, world_size: int) -> Layout:
     out = _LAYOUT()
     _check(_lib.fsdp_plan_layout_host(arr, len(params), world_size, ctypes.byref(out)),
            "fsdp_plan_layout_host")
-    return Layout(out.value, len(params))
+    return Layout(out.value, len(params), arr)
 
 
 def fsdp_plan_layout_ex(params, world_size: int, row_elems=None, flags: int = 0) -> Layout:
@@ -189,7 +196,7 @@ def fsdp_plan_layout_ex(params, world_size: int, row_elems=None, flags: int = 0)
     out = _LAYOUT()
     _check(_lib.fsdp_plan_layout_ex(arr, rows, len(params), world_size, flags, ctypes.byref(out)),
            "fsdp_plan_layout_ex")
-    return Layout(out.value, len(params))
+    return Layout(out.value, len(params), arr)
 
 
 def row_elems_of(specs):
@@ -227,6 +234,99 @@ def fsdp_layout_group(layout: Layout, g: int) -> fsdp_group_info_t:
     return info
 
 
+# ---------------------------------------------------------------------------
+# Argument checks.  The C ABI takes bare pointers and reads as many as the
+# layout has slots, so the binding checks what it can before the call: the
+# number of pointers always, and for torch tensors their size, dtype,
+# contiguity and device.  Integers and prebuilt pointer arrays are passed
+# through unchecked beyond their count.
+# ---------------------------------------------------------------------------
+def _layout_slots(layout: Layout) -> dict:
+    """Per slot list of one operation: (bytes, dtype code or None) of each slot."""
+    if layout._slots is None:
+        info = fsdp_layout_query(layout)
+        W, d = info.world_size, layout.descs
+        prm = [fsdp_layout_param(layout, p) for p in range(info.n_params)]
+        bkt = [fsdp_layout_bucket(layout, b) for b in range(info.n_buckets)]
+        sz = DTYPE_BYTES
+        layout._slots = {
+            "grads": [(n * sz[g], g) for n, g, _, _, _ in d],
+            "buckets": [(b.bytes, b.reduce_dtype) for b in bkt],
+            "shards": [(q.chunk * sz[x[3]], x[3]) for q, x in zip(prm, d)],
+            "ag_input": [(info.ag_bytes, None)],
+            "ag_output": [(W * info.ag_bytes, None)],
+            "full": [(x[0] * sz[x[4]], x[4]) for x in d],
+            "rows": [(b.row_elems * sz[b.reduce_dtype], b.reduce_dtype) for b in bkt],
+            "sharded": [(q.chunk * sz[x[3]], x[3]) for q, x in zip(prm, d)],
+            "packed": [(b.bytes, b.reduce_dtype) for b in bkt for _ in range(W)],
+            "reduced": [(b.bytes, b.reduce_dtype) for b in bkt],
+            "device": info.device if info.has_device_table else None,
+        }
+    return layout._slots
+
+
+def _torch_dtype_code(t):
+    import torch
+    return {torch.float32: FSDP_DTYPE_F32, torch.bfloat16: FSDP_DTYPE_BF16}.get(t.dtype, "other")
+
+
+def _check_args(where: str, what: str, ts, slots, device, placement: bool) -> None:
+    """Raise ValueError if ``ts`` (a list, a tensor or int for a single slot,
+    or a prebuilt pointer array) does not fit ``slots``: counts, sizes,
+    dtypes and contiguity, or with ``placement`` the tensors' devices."""
+    if ts is None or isinstance(ts, int):
+        return
+    if isinstance(ts, ctypes.Array):
+        if len(slots) > len(ts):
+            raise ValueError(f"{where}: {what} holds {len(ts)} pointers, the layout needs {len(slots)}")
+        return
+    single = not isinstance(ts, (list, tuple))
+    items = [ts] if single else list(ts)
+    if len(items) != len(slots):
+        raise ValueError(f"{where}: {len(items)} {what} given, the layout has {len(slots)}")
+    for k, (t, (need, dt)) in enumerate(zip(items, slots)):
+        if t is None or isinstance(t, int) or not hasattr(t, "data_ptr"):
+            continue
+        name = what if single else f"{what}[{k}]"
+        if placement:
+            if need and not t.is_cuda:
+                raise ValueError(f"{where}: {name} is not a CUDA tensor")
+            if need and device is not None and t.device.index != device:
+                raise ValueError(f"{where}: {name} is on cuda:{t.device.index}, the layout on cuda:{device}")
+            continue
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} is not contiguous")
+        have = t.numel() * t.element_size()
+        if have < need:
+            raise ValueError(f"{where}: {name} holds {have} bytes, the layout needs {need}")
+        if dt is not None and t.is_floating_point() and _torch_dtype_code(t) != dt:
+            raise ValueError(f"{where}: {name} is {t.dtype}, the layout's dtype is "
+                             f"{'f32' if dt == FSDP_DTYPE_F32 else 'bf16'} (pass raw bits as an integer tensor)")
+
+
+def _check_lists(where: str, slots: dict, lists: dict) -> None:
+    for placement in (False, True):  # every count, size and dtype first, then devices
+        for what, ts in lists.items():
+            _check_args(where, what, ts, slots.get(what, []), slots["device"], placement)
+
+
+def _check_layout_args(where: str, layout: Layout, **lists) -> None:
+    if not isinstance(layout, Layout) or not layout.handle:
+        return  # the C call reports a null or closed layout
+    _check_lists(where, _layout_slots(layout), lists)
+
+
+def _check_batched_args(where: str, la: "LayoutArray", **lists) -> None:
+    if not all(isinstance(L, Layout) and L.handle for L in la.layouts):
+        return  # the C call reports a null or closed layout
+    if la.slots is None:  # the layouts' slot lists concatenated, once per array
+        per = [_layout_slots(L) for L in la.layouts]
+        devices = {s["device"] for s in per}
+        la.slots = {k: [x for s in per for x in s[k]] for k in per[0] if k != "device"} if per else {}
+        la.slots["device"] = devices.pop() if len(devices) == 1 else None
+    _check_lists(where, la.slots, lists)
+
+
 def _ptr(t) -> int | None:
     if t is None:
         return None
@@ -256,21 +356,25 @@ def _stream(stream) -> int | None:
 
 
 def fsdp_pack_reduce_scatter(layout: Layout, grads, bucket_bufs, stream=None) -> None:
+    _check_layout_args("fsdp_pack_reduce_scatter", layout, grads=grads, buckets=bucket_bufs)
     _check(_lib.fsdp_pack_reduce_scatter(layout.handle, pointer_array(grads), pointer_array(bucket_bufs),
                                          _stream(stream)), "fsdp_pack_reduce_scatter")
 
 
 def fsdp_allgather_copy_in(layout: Layout, local_shards, ag_input, stream=None) -> None:
+    _check_layout_args("fsdp_allgather_copy_in", layout, shards=local_shards, ag_input=ag_input)
     _check(_lib.fsdp_allgather_copy_in(layout.handle, pointer_array(local_shards), _ptr(ag_input),
                                        _stream(stream)), "fsdp_allgather_copy_in")
 
 
 def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None) -> None:
+    _check_layout_args("fsdp_allgather_copy_out", layout, ag_output=ag_output, full=full_params)
     _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), pointer_array(full_params),
                                         _stream(stream)), "fsdp_allgather_copy_out")
 
 
 def fsdp_reduce_scatter_copy_out(layout: Layout, reduced_rows, sharded_grads, stream=None) -> None:
+    _check_layout_args("fsdp_reduce_scatter_copy_out", layout, rows=reduced_rows, sharded=sharded_grads)
     _check(_lib.fsdp_reduce_scatter_copy_out(layout.handle, pointer_array(reduced_rows), pointer_array(sharded_grads),
                                              _stream(stream)), "fsdp_reduce_scatter_copy_out")
 
@@ -278,6 +382,7 @@ def fsdp_reduce_scatter_copy_out(layout: Layout, reduced_rows, sharded_grads, st
 def fsdp_emulated_reduce_scatter(layout: Layout, packed, reduced, stream=None) -> None:
     """packed: n_buckets * W pointers, bucket-major (packed[b*W + q] = rank q's
     bucket b); reduced: one [W, S_b] buffer per bucket."""
+    _check_layout_args("fsdp_emulated_reduce_scatter", layout, packed=packed, reduced=reduced)
     _check(_lib.fsdp_emulated_reduce_scatter(layout.handle, pointer_array(packed), pointer_array(reduced),
                                              _stream(stream)), "fsdp_emulated_reduce_scatter")
 
@@ -288,6 +393,8 @@ class LayoutArray:
 
     def __init__(self, layouts):
         self.n = len(layouts)
+        self.layouts = list(layouts)
+        self.slots = None
         self.arr = (_LAYOUT * max(1, self.n))()
         for k, L in enumerate(layouts):
             self.arr[k] = L.handle
@@ -300,6 +407,7 @@ def layout_array(layouts) -> LayoutArray:
 def fsdp_pack_reduce_scatter_batched(layouts, grads, bucket_bufs, stream=None) -> None:
     """grads / bucket_bufs: the per-layout lists concatenated in layout order."""
     la = layout_array(layouts)
+    _check_batched_args("fsdp_pack_reduce_scatter_batched", la, grads=grads, buckets=bucket_bufs)
     _check(_lib.fsdp_pack_reduce_scatter_batched(la.arr, la.n, pointer_array(grads), pointer_array(bucket_bufs),
                                                  _stream(stream)),
            "fsdp_pack_reduce_scatter_batched")
@@ -308,6 +416,7 @@ def fsdp_pack_reduce_scatter_batched(layouts, grads, bucket_bufs, stream=None) -
 def fsdp_allgather_copy_in_batched(layouts, local_shards, ag_inputs, stream=None) -> None:
     """local_shards concatenated in layout order; one ag_input per layout."""
     la = layout_array(layouts)
+    _check_batched_args("fsdp_allgather_copy_in_batched", la, shards=local_shards, ag_input=ag_inputs)
     _check(_lib.fsdp_allgather_copy_in_batched(la.arr, la.n, pointer_array(local_shards), pointer_array(ag_inputs),
                                                _stream(stream)),
            "fsdp_allgather_copy_in_batched")
@@ -316,6 +425,7 @@ def fsdp_allgather_copy_in_batched(layouts, local_shards, ag_inputs, stream=None
 def fsdp_allgather_copy_out_batched(layouts, ag_outputs, full_params, stream=None) -> None:
     """One ag_output per layout; full_params concatenated in layout order."""
     la = layout_array(layouts)
+    _check_batched_args("fsdp_allgather_copy_out_batched", la, ag_output=ag_outputs, full=full_params)
     _check(_lib.fsdp_allgather_copy_out_batched(la.arr, la.n, pointer_array(ag_outputs), pointer_array(full_params),
                                                 _stream(stream)),
            "fsdp_allgather_copy_out_batched")
@@ -324,6 +434,7 @@ def fsdp_allgather_copy_out_batched(layouts, ag_outputs, full_params, stream=Non
 def fsdp_reduce_scatter_copy_out_batched(layouts, reduced_rows, sharded_grads, stream=None) -> None:
     """reduced_rows / sharded_grads: the per-layout lists concatenated in layout order."""
     la = layout_array(layouts)
+    _check_batched_args("fsdp_reduce_scatter_copy_out_batched", la, rows=reduced_rows, sharded=sharded_grads)
     _check(_lib.fsdp_reduce_scatter_copy_out_batched(la.arr, la.n, pointer_array(reduced_rows),
                                                      pointer_array(sharded_grads), _stream(stream)),
            "fsdp_reduce_scatter_copy_out_batched")
@@ -331,6 +442,7 @@ def fsdp_reduce_scatter_copy_out_batched(layouts, reduced_rows, sharded_grads, s
 
 def fsdp_pack_reduce_scatter_noalloc(layout: Layout, grads, bucket_bufs, stream=None) -> None:
     """The pack with its scratch in the library's static array (no allocation)."""
+    _check_layout_args("fsdp_pack_reduce_scatter_noalloc", layout, grads=grads, buckets=bucket_bufs)
     _check(_lib.fsdp_pack_reduce_scatter_noalloc(layout.handle, pointer_array(grads), pointer_array(bucket_bufs),
                                                  _stream(stream)), "fsdp_pack_reduce_scatter_noalloc")
 

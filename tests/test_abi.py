@@ -177,6 +177,59 @@ def test_batched_calls_check_their_arguments_without_launching(fp):
             L.close()
 
 
+def test_binding_checks_pointer_counts_and_tensors_before_calling(fp):
+    """The C entry points read as many pointers as the layout has slots, so
+    the binding refuses short lists (and short prebuilt arrays) of any kind,
+    and checks torch tensors against the layout: size, floating dtype,
+    contiguity, device.  All of it happens before the C call."""
+    import torch
+    specs = wl.tiny_two_blocks(grouping="block").groups[1]       # BF16 grads, FP32 bucket
+    W = 4
+    with fp.fsdp_plan_layout_host(specs, W) as L:
+        b = fp.fsdp_layout_bucket(L, 0)
+        grads = [torch.zeros(s.numel, dtype=torch.bfloat16) for s in specs]
+        bucket = torch.zeros(b.bytes // 4, dtype=torch.float32)
+        cases = [
+            (([grads[0]], [bucket]), "1 grads given, the layout has 2"),
+            (([0x1000], [0x2000]), "1 grads given, the layout has 2"),
+            ((fp.pointer_array([0x1000]), [bucket]), "holds 1 pointers, the layout needs 2"),
+            (([grads[0], grads[1][:-1]], [bucket]), "grads[1] holds 70 bytes, the layout needs 72"),
+            (([grads[0], grads[1].float()], [bucket]), "grads[1] is torch.float32, the layout's dtype is bf16"),
+            ((grads, [bucket[:-1]]), f"buckets[0] holds {b.bytes - 4} bytes, the layout needs {b.bytes}"),
+            ((grads, [torch.zeros(b.bytes // 2, dtype=torch.bfloat16)]),
+             "buckets[0] is torch.bfloat16, the layout's dtype is f32"),
+            ((grads, [torch.zeros(2 * (b.bytes // 4), dtype=torch.float32)[::2]]), "buckets[0] is not contiguous"),
+            ((grads, [bucket]), "grads[0] is not a CUDA tensor"),
+            (([g.view(torch.int16) for g in grads], [bucket.view(torch.uint8)]), "grads[0] is not a CUDA tensor"),
+        ]
+        for args, msg in cases:
+            with pytest.raises(ValueError, match=re.escape(msg)):
+                fp.fsdp_pack_reduce_scatter(L, *args, stream=0)
+        c = [fp.fsdp_layout_param(L, p).chunk for p in range(2)]
+        S_ag = fp.fsdp_layout_query(L).ag_bytes
+        with pytest.raises(ValueError, match="ag_input holds 8 bytes"):
+            fp.fsdp_allgather_copy_in(L, [torch.zeros(ci) for ci in c], torch.zeros(2), stream=0)
+        with pytest.raises(ValueError, match=re.escape(f"ag_output holds {W * S_ag - 1} bytes")):
+            fp.fsdp_allgather_copy_out(L, torch.zeros(W * S_ag - 1, dtype=torch.uint8), [0x1000, 0x2000], stream=0)
+        with pytest.raises(ValueError, match="full\\[1\\] is torch.float32, the layout's dtype is bf16"):
+            fp.fsdp_allgather_copy_out(L, 0x1000, [torch.zeros(36, dtype=torch.bfloat16), torch.zeros(36)], stream=0)
+        with pytest.raises(ValueError, match="3 rows given, the layout has 1"):
+            fp.fsdp_reduce_scatter_copy_out(L, [0x1000] * 3, [0x2000] * 2, stream=0)
+        with pytest.raises(ValueError, match=f"{W - 1} packed given, the layout has {W}"):
+            fp.fsdp_emulated_reduce_scatter(L, [0x1000] * (W - 1), [0x2000], stream=0)
+        with pytest.raises(ValueError, match="1 grads given, the layout has 2"):
+            fp.fsdp_pack_reduce_scatter_noalloc(L, [0x1000], [0x2000], stream=0)
+        # Batched: the lists are the layouts' lists concatenated.
+        with pytest.raises(ValueError, match="3 grads given, the layout has 4"):
+            fp.fsdp_pack_reduce_scatter_batched([L, L], [0x1000] * 3, [0x2000] * 2, stream=0)
+        with pytest.raises(ValueError, match="grads\\[3\\] holds 70 bytes"):
+            fp.fsdp_pack_reduce_scatter_batched(fp.layout_array([L, L]), grads + [grads[0], grads[1][:-1]],
+                                                [bucket, bucket], stream=0)
+        # Right counts of plain integers reach the library, which refuses a host-only layout.
+        with pytest.raises(fp.FsdpError):
+            fp.fsdp_pack_reduce_scatter(L, [0x1000, 0x2000], [0x3000], stream=0)
+
+
 def test_query_index_out_of_range(fp):
     with fp.fsdp_plan_layout_host(wl.tiny_two_blocks().groups[0], 4) as L:
         for fn in (fp.fsdp_layout_param, fp.fsdp_layout_bucket, fp.fsdp_layout_group):

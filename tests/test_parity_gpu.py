@@ -374,6 +374,49 @@ def test_calls_replay_from_a_cuda_graph(fp):
         run.close()
 
 
+def test_torch_tensors_of_the_layout_dtypes_are_accepted_and_checked(fp):
+    """Callers may pass float32 / bfloat16 tensors (and byte tensors for the
+    all-gather buffers): correct ones give the oracle's results, a tensor
+    smaller than its slot is refused before anything is launched."""
+    work = wl.tiny_two_blocks(grouping="model")
+    specs, W = work.groups[0], 4
+    pl = oracle.plan(oracle.params_from_specs(specs), W)
+    tdt = {"f32": (np.int32, torch.float32), "bf16": (np.int16, torch.bfloat16)}
+
+    def dev(bits, dt):
+        return torch.from_numpy(bits.view(tdt[dt][0]).copy()).cuda().view(tdt[dt][1])
+
+    grads_np = [wl.grad_values(work, 0, i) for i in range(len(specs))]
+    grads = [dev(g, s.grad_dtype) for g, s in zip(grads_np, specs)]
+    S = pl.bucket_S[0]
+    with fp.fsdp_plan_layout(specs, W) as L:
+        bucket = torch.full((W * S,), float("nan"), device="cuda")
+        fp.fsdp_pack_reduce_scatter(L, grads, [bucket])
+        got = bucket.view(torch.int32).cpu().numpy().view(np.uint32)
+        want, = oracle.pack_reduce_scatter(pl, grads_np)
+        assert np.array_equal(got, want), first_mismatch(got, want)
+
+        short = torch.full((W * S - 1,), 7.0, device="cuda")
+        with pytest.raises(ValueError, match="holds"):
+            fp.fsdp_pack_reduce_scatter(L, grads, [short])
+        torch.cuda.synchronize()
+        assert bool((short == 7.0).all())
+
+        shards_np = [[wl.shard_values(work, 0, i, r, c, min(c, s.numel - r * c))
+                      for i, (c, s) in enumerate(zip(pl.chunk, specs))] for r in range(W)]
+        gathered = torch.full((W * pl.S_ag,), 0xA5, dtype=torch.uint8, device="cuda")
+        for r in range(W):
+            fp.fsdp_allgather_copy_in(L, [dev(x, s.shard_dtype) for x, s in zip(shards_np[r], specs)],
+                                      gathered[r * pl.S_ag:(r + 1) * pl.S_ag])
+        want_rows = np.concatenate([oracle.allgather_copy_in(pl, shards_np[r]) for r in range(W)])
+        assert np.array_equal(gathered.cpu().numpy(), want_rows)
+        full = [torch.empty(s.numel, dtype=tdt[s.param_dtype][1], device="cuda") for s in specs]
+        fp.fsdp_allgather_copy_out(L, gathered, full)
+        for t, s, w in zip(full, specs, oracle.allgather_copy_out(pl, want_rows)):
+            got = t.view({"f32": torch.int32, "bf16": torch.int16}[s.param_dtype]).cpu().numpy().view(NP[s.param_dtype])
+            assert np.array_equal(got, w), first_mismatch(got, w)
+
+
 def test_empty_layout_and_empty_parameters(fp):
     with fp.fsdp_plan_layout([], 8) as L:
         fp.fsdp_pack_reduce_scatter(L, [], [])
