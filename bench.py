@@ -359,6 +359,26 @@ class OracleSampler:
         return nbytes
 
 
+def host_cpu() -> dict:
+    """The host the CPU legs run on: logical CPUs and the CPU model as
+    /proc/cpuinfo names it (Arm hosts give implementer and part numbers)."""
+    model = None
+    try:
+        fields = {}
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+        model = fields.get("model name") or (
+            f"implementer {fields['CPU implementer']} part {fields['CPU part']}"
+            if "CPU implementer" in fields and "CPU part" in fields else None)
+    except OSError:
+        pass
+    import platform
+    return {"host_cpus": os.cpu_count(), "cpu_model": model, "machine": platform.machine(),
+            "threads_used": 1}
+
+
 def cpu_baseline(sampler: OracleSampler, seconds: float) -> dict:
     """Whole steps of the oracle (all segments in order) for about `seconds`."""
     done_bytes, steps = 0, 0
@@ -372,7 +392,7 @@ def cpu_baseline(sampler: OracleSampler, seconds: float) -> dict:
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{steps} whole step(s) of the same workload (pack, copy-in of one rank, copy-out), "
-                      f"single-threaded C oracle, {dt:.1f} s"}
+                      f"single-threaded C oracle, {dt:.1f} s", **host_cpu()}
 
 
 # ---------------------------------------------------------------------------
@@ -842,7 +862,7 @@ def run_reference(args):
                    "groups": len(work.groups), "step_bytes": samp.step_bytes, "parallelism": "single host thread"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "each step = one (rank, parameter) run of the pack, copy-in or copy-out, "
-                                   f"cycling through the {len(samp.segs)} runs of a whole step"},
+                                   f"cycling through the {len(samp.segs)} runs of a whole step", **host_cpu()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(result), flush=True)
