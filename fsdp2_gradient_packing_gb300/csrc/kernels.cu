@@ -29,8 +29,10 @@
 //     written one by one straight from global memory;
 //   * consumers release the stage on its "empty" mbarrier; the producer
 //     reuses it kStages items later.
-// FP32 -> BF16 rounding is done on the bits (round to nearest, ties to even),
-// so results do not depend on the device's FP modes.
+// FP32 -> BF16 rounding in walk_kernel is done on the bits (round to nearest,
+// ties to even), so results do not depend on the device's FP modes; the
+// vector path of sum_kernel rounds BF16 pairs with the hardware's
+// round-to-nearest-even conversion, which gives the same bits.
 //
 // Every mbarrier wait is bounded (a limit in nanoseconds of %globaltimer).  A
 // wait that gives up sets a bit in the layout's device status word and the
@@ -614,8 +616,8 @@ __device__ __forceinline__ uint32_t add_bf16_pair(uint32_t x, uint32_t y) {
 template <bool BF16>
 __device__ __forceinline__ uint4 add_vec(uint4 a, uint4 b) {
   if constexpr (BF16) {
-    auto pair = [](uint32_t x, uint32_t y) { return add_bf16_pair(x, y); };
-    return make_uint4(pair(a.x, b.x), pair(a.y, b.y), pair(a.z, b.z), pair(a.w, b.w));
+    return make_uint4(add_bf16_pair(a.x, b.x), add_bf16_pair(a.y, b.y), add_bf16_pair(a.z, b.z),
+                      add_bf16_pair(a.w, b.w));
   } else {
     return make_uint4(add_bits<false>(a.x, b.x), add_bits<false>(a.y, b.y), add_bits<false>(a.z, b.z),
                       add_bits<false>(a.w, b.w));
