@@ -38,6 +38,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import shutil
 import statistics
@@ -56,7 +57,8 @@ from fsdp2_gradient_packing_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "reduce-scatter pack GB/s and ms per fully_shard (50.3M elem, W=8) vs HBM peak"
 UNIT = "GB/s"
-NOMINAL_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the metric is quoted against
+NOMINAL_HBM_GBS = 8000.0
+CHUNKING = {False: "flattened: c_p = ceil(n_p / W)", True: "dim-0 rows: c_p = ceil(d0 / W) * row elements"}   # the "~8 TB/s" HBM figure the metric is quoted against
 FALLBACK_HBM_GBS = 6800.0
 ESZ = {"f32": 4, "bf16": 2}
 STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
@@ -73,6 +75,9 @@ WORKLOADS = {
     "transformer500_homogeneous": (lambda: wl.transformer_500(W=8, homogeneous=True),
                                    "transformer500_W8 with param dtype BF16 for every parameter (one all-gather "
                                    "dtype group): the homogeneous counterpart of transformer500"),
+    "mixed50m_w12": (lambda: wl.mixed_50m(W=12),
+                     "mixed50m_W12: the mixed50m group at W=12, which divides no matrix's dim 0 "
+                     "(1024, 4096), so flattened and dim-0 row chunks differ"),
     "kda8": (lambda: wl.kda_block(W=8, reduce="f32", blocks=8),
              "kda8_W8: all 8 KDA-style blocks (1,744,929,024 parameters), one fully_shard group per block, W=8"),
     "kda8_homogeneous": (lambda: wl.kda_block(W=8, reduce="f32", blocks=8, homogeneous=True),
@@ -108,6 +113,8 @@ def parse_args(argv=None):
                     help="add the emulated reduce-scatter (sum of W ranks' packed buffers) after the pack")
     ap.add_argument("--precast-iters", type=int, default=200,
                     help="iterations of the pre-cast-then-pack comparison (0 = skip)")
+    ap.add_argument("--row-chunks", action="store_true",
+                    help="plan every parameter by dim-0 rows (c_p = ceil(d0 / W) rows) instead of flattened")
     ap.add_argument("--graph", action="store_true",
                     help="time the step as replays of a CUDA graph holding two steps (both buffer sets)")
     ap.add_argument("--batched", action="store_true",
@@ -152,12 +159,21 @@ def max_over_ranks(x: float, device=None) -> float:
 # ---------------------------------------------------------------------------
 # Workload sizes.
 # ---------------------------------------------------------------------------
-def chunks(specs, W):
-    return [-(-s.numel // W) for s in specs]
+def row_elems(specs):
+    """Elements of one dim-0 row of each parameter (1 for 1-D parameters)."""
+    return [math.prod(s.shape[1:]) if len(s.shape) > 1 else 1 for s in specs]
 
 
-def op_bytes(specs, W, bucket_bytes, S_ag):
-    c = chunks(specs, W)
+def chunks(specs, W, rows=False):
+    """c_p of every parameter: ceil(n_p / W) of the flattened parameter, or
+    with ``rows`` ceil(d0 / W) whole dim-0 rows."""
+    if not rows:
+        return [-(-s.numel // W) for s in specs]
+    return [(-(-s.shape[0] // W) * r if s.numel else 0) for s, r in zip(specs, row_elems(specs))]
+
+
+def op_bytes(specs, W, bucket_bytes, S_ag, rows=False):
+    c = chunks(specs, W, rows)
     pack = sum(s.numel * ESZ[s.grad_dtype] for s in specs) + sum(bucket_bytes)
     copy_in = sum(ci * ESZ[s.shard_dtype] for ci, s in zip(c, specs)) + S_ag
     copy_out = 2 * sum(s.numel * ESZ[s.param_dtype] for s in specs)
@@ -279,10 +295,10 @@ def flat_offsets(sizes, align=256):
     return offs, max(at, align)
 
 
-def host_inputs(work, g):
+def host_inputs(work, g, rows=False):
     """Seeded gradients and every rank's shards of group g."""
     specs, W = work.groups[g], work.W
-    c = chunks(specs, W)
+    c = chunks(specs, W, rows)
     grads = [wl.grad_values(work, g, i) for i in range(len(specs))]
     shards = [[wl.shard_values(work, g, i, r, c[i], max(0, min(c[i], s.numel - r * c[i])))
                for i, s in enumerate(specs)] for r in range(W)]
@@ -305,14 +321,14 @@ class OracleSampler:
     (pack runs, copy-in runs of rank 0, copy-out runs), each with its
     algorithmic bytes."""
 
-    def __init__(self, work, inputs):
+    def __init__(self, work, inputs, rows=False):
         import oracle
         self.oracle = oracle
         W = work.W
         self.segs = []
         for g, specs in enumerate(work.groups):
             grads, shards = inputs[g]
-            pl = oracle.plan(oracle.params_from_specs(specs), W)
+            pl = oracle.plan(oracle.params_from_specs(specs), W, row_elems=row_elems(specs) if rows else None)
             st = {
                 "pl": pl, "grads": grads, "shards0": shards[0],
                 "bufs": [np.empty(W * S, oracle.DTYPE_NP[d]) for d, S in zip(pl.bucket_dtype, pl.bucket_S)],
@@ -401,9 +417,9 @@ def cpu_baseline(sampler: OracleSampler, seconds: float) -> dict:
 class DeviceSet:
     """One complete set of device buffers for a step (two sets rotate)."""
 
-    def __init__(self, fp, torch, L, specs, W, info, host_grads, host_shards, rank_row, others=None):
+    def __init__(self, fp, torch, L, specs, W, info, host_grads, host_shards, rank_row, others=None, rows=False):
         dev = torch.device("cuda")
-        c = chunks(specs, W)
+        c = chunks(specs, W, rows)
         self.S_ag = info.ag_bytes
         g_sizes = [s.numel * ESZ[s.grad_dtype] for s in specs]
         goffs, gtot = flat_offsets(g_sizes)
@@ -478,18 +494,19 @@ class DeviceSet:
 class Group:
     """One fully_shard group on the device: its layout and two buffer sets."""
 
-    def __init__(self, fp, torch, work, g, inputs, emulated_rs=False):
+    def __init__(self, fp, torch, work, g, inputs, emulated_rs=False, rows=False):
         self.specs = work.groups[g]
-        self.L = fp.fsdp_plan_layout(self.specs, work.W)
+        self.L = (fp.fsdp_plan_layout_ex(self.specs, work.W, row_elems(self.specs)) if rows
+                  else fp.fsdp_plan_layout(self.specs, work.W))
         self.info = fp.fsdp_layout_query(self.L)
         bucket_bytes = [fp.fsdp_layout_bucket(self.L, b).bytes for b in range(self.info.n_buckets)]
-        self.nbytes = op_bytes(self.specs, work.W, bucket_bytes, self.info.ag_bytes)
+        self.nbytes = op_bytes(self.specs, work.W, bucket_bytes, self.info.ag_bytes, rows)
         grads, shards = inputs
         others = None
         if emulated_rs:   # the other ranks' packed buffers (contents do not matter for timing)
             others = [[torch.zeros(n, dtype=torch.uint8, device="cuda") for _ in range(work.W - 1)]
                       for n in bucket_bytes]
-        self.sets = [DeviceSet(fp, torch, self.L, self.specs, work.W, self.info, grads, shards, 0, others)
+        self.sets = [DeviceSet(fp, torch, self.L, self.specs, work.W, self.info, grads, shards, 0, others, rows)
                      for _ in range(2)]
 
 
@@ -528,7 +545,7 @@ class Batch:
                 ev[4].record()
 
 
-def precast_comparison(fp, torch, work, grp, h, iters):
+def precast_comparison(fp, torch, work, grp, h, iters, rows=False):
     """The sequence the fused pack replaces: every BF16 gradient that reduces in
     FP32 is first cast into one FP32 temporary, then an FP32 -> FP32 pack reads
     the temporary ("FSDP2 per-parameter mixed precision", results table:
@@ -546,7 +563,9 @@ def precast_comparison(fp, torch, work, grp, h, iters):
     cast_specs = [dataclasses.replace(specs[i], reduce_dtype="f32") for i in cast_idx]
     fp32_specs = [dataclasses.replace(s, grad_dtype="f32") if i in set(cast_idx) else s
                   for i, s in enumerate(specs)]
-    with fp.fsdp_plan_layout(cast_specs, 1) as L_cast, fp.fsdp_plan_layout(fp32_specs, work.W) as L32:
+    L32 = (fp.fsdp_plan_layout_ex(fp32_specs, work.W, row_elems(fp32_specs)) if rows
+           else fp.fsdp_plan_layout(fp32_specs, work.W))
+    with fp.fsdp_plan_layout(cast_specs, 1) as L_cast, L32:
         tmp_bytes = fp.fsdp_layout_bucket(L_cast, 0).bytes
         tmp = torch.empty(tmp_bytes, dtype=torch.uint8, device="cuda")
         offs = {i: fp.fsdp_layout_param(L_cast, k).bucket_offset * 4 for k, i in enumerate(cast_idx)}
@@ -584,7 +603,7 @@ def precast_comparison(fp, torch, work, grp, h, iters):
             fp.fsdp_sync_status(L)
         bucket_bytes = [fp.fsdp_layout_bucket(L32, b).bytes for b in range(fp.fsdp_layout_query(L32).n_buckets)]
         pre_bytes = (op_bytes(cast_specs, 1, [tmp_bytes], 0)["pack"]
-                     + op_bytes(fp32_specs, work.W, bucket_bytes, 0)["pack"])
+                     + op_bytes(fp32_specs, work.W, bucket_bytes, 0, rows)["pack"])
         del tmp
     return {"what": "BF16 gradients cast into one FP32 temporary, then the FP32 -> FP32 pack, "
                     "against the fused pack; back-to-back loops of " + str(iters),
@@ -613,8 +632,9 @@ def run_ours(args):
     init_dist("nccl" if world > 1 else "gloo")
     factory, description = WORKLOADS[args.workload]
     work = factory()
-    inputs = [host_inputs(work, g) for g in range(len(work.groups))]
-    groups = [Group(fp, torch, work, g, inputs[g], args.emulated_rs) for g in range(len(work.groups))]
+    rows = args.row_chunks
+    inputs = [host_inputs(work, g, rows) for g in range(len(work.groups))]
+    groups = [Group(fp, torch, work, g, inputs[g], args.emulated_rs, rows) for g in range(len(work.groups))]
     if args.batched and args.emulated_rs:
         raise SystemExit("--emulated-rs has no batched form; drop --batched")
     OPS = (("pack",) + (("emulated_rs",) if args.emulated_rs else ()) + ("copy_in", "copy_out")
@@ -686,7 +706,7 @@ def run_ours(args):
 
     precast = None
     if len(groups) == 1 and args.precast_iters > 0:
-        precast = precast_comparison(fp, torch, work, groups[0], h, args.precast_iters)
+        precast = precast_comparison(fp, torch, work, groups[0], h, args.precast_iters, rows)
 
     e2e = None
     if args.e2e_steps > 0:
@@ -701,7 +721,7 @@ def run_ours(args):
     for grp in groups:
         grp.L.close()
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        samp = OracleSampler(work, inputs)
+        samp = OracleSampler(work, inputs, rows)
         result["cpu_baseline"] = cpu_baseline(samp, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -812,6 +832,7 @@ def report(args, work, description, groups, nbytes, step_bytes, total_ms, per, c
         "data": "synthetic",
         "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else "")
                    + (STEP_ERS if args.emulated_rs else ""), "world_size_layout": work.W,
+                   "chunking": CHUNKING[args.row_chunks],
                    "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
                    "launch": ("CUDA graph of two steps, replayed" if args.graph
                               else "stream launches from the host") + (", batched over groups" if args.batched else ""),
@@ -843,8 +864,8 @@ def run_reference(args):
         return
     factory, description = WORKLOADS[args.workload]
     work = factory()
-    inputs = [host_inputs(work, g) for g in range(len(work.groups))]
-    samp = OracleSampler(work, inputs)
+    inputs = [host_inputs(work, g, args.row_chunks) for g in range(len(work.groups))]
+    samp = OracleSampler(work, inputs, args.row_chunks)
     for _ in range(args.warmup):
         samp.next()
     done = 0
@@ -859,6 +880,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32", "data": "synthetic",
         "config": {"workload": f"{description}; {STEP}", "world_size_layout": work.W,
+                   "chunking": CHUNKING[args.row_chunks],
                    "groups": len(work.groups), "step_bytes": samp.step_bytes, "parallelism": "single host thread"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "each step = one (rank, parameter) run of the pack, copy-in or copy-out, "
