@@ -15,18 +15,18 @@
 // pipeline built to keep many bytes in flight per SM with few registers and
 // to write only full, aligned 16-byte vectors:
 //   * warp 0, lane 0 is the producer.  For each item of its CTA it copies the
-//     16-byte-aligned interior of the item's source bytes into one stage of a
-//     shared-memory ring with one TMA bulk copy (cp.async.bulk), completion
-//     counted on that stage's "full" mbarrier;
+//     item's source bytes, widened to whole aligned 16-byte blocks, into one
+//     stage of a shared-memory ring with one TMA bulk copy (cp.async.bulk),
+//     completion counted on that stage's "full" mbarrier;
 //   * warps 1..8 are consumers.  For each item they wait on the stage, then
 //     write the destination as 16-byte vectors: each lane reads the source
 //     bytes of one vector from shared memory at whatever byte phase they have
 //     (word loads plus a funnel shift), converts them and stores one aligned
 //     16-byte vector, so every warp store covers 512 contiguous bytes.  Vectors
 //     made only of padding are stored as zeros without reading anything.
-//     The few elements outside the staged interior (a run's ragged ends, and
-//     the destination's head before its first 16-byte boundary) are read and
-//     written one by one straight from global memory;
+//     The destination's head before its first 16-byte boundary, its tail, and
+//     the one vector where valid data meets padding are written element by
+//     element, also from the stage: consumers never read global memory;
 //   * consumers release the stage on its "empty" mbarrier; the producer
 //     reuses it kStages items later.
 // FP32 -> BF16 rounding in walk_kernel is done on the bits (round to nearest,
@@ -56,10 +56,12 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kStages = 4;
-// Each stage holds a 64-byte header (the item, see StageHeader) and
-// kStageBytes of data plus 16 bytes of slack: the funnel read of the last
-// vector may touch one word past the staged bytes.
-constexpr int kStageStride = 64 + (int)kStageBytes + 16;
+// Each stage holds a 64-byte header (the item, see StageHeader) and the
+// item's staged source: its source bytes widened to whole aligned 16-byte
+// blocks, at most kStageBytes + 16 bytes.  The funnel read of the last vector
+// may touch one word past them, hence 32 bytes of slack in all.
+constexpr int kStagedMax = (int)kStageBytes + 16;
+constexpr int kStageStride = 64 + (int)kStageBytes + 32;
 constexpr int kSmemBytes = kStages * kStageStride + 2 * kStages * 8;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -246,29 +248,32 @@ __device__ __forceinline__ uint32_t convert_one(uint32_t x) {
   else return x;
 }
 
+// Destination element k of an item, written alone: source element k from the
+// stage (cast), or +0 past n_copy.
 template <int KIND>
-__device__ __forceinline__ void scalar_elem(const char *src, char *dst, int k, int n_copy) {
+__device__ __forceinline__ void scalar_elem(const uint8_t *stage, int lead, char *dst, int k, int n_copy) {
   using S = typename Traits<KIND>::S;
   using D = typename Traits<KIND>::D;
   uint32_t v = 0;
-  if (k < n_copy) v = convert_one<KIND>((uint32_t)reinterpret_cast<const S *>(src)[k]);
+  if (k < n_copy) v = convert_one<KIND>((uint32_t)*reinterpret_cast<const S *>(stage + lead + k * (int)sizeof(S)));
   reinterpret_cast<D *>(dst)[k] = (D)v;
 }
 
-// Source interior of an item that is staged in shared memory: bytes
-// [lo, hi) counted from the item's first source byte, where lo is the first
-// 16-byte boundary (or the end, for a run too short to have one) and hi - lo
-// is the largest multiple of 16 that fits.
-struct Interior {
-  int lo, hi;
+// The staged source of an item: the aligned 16-byte blocks that hold its
+// valid source bytes [src, src + src_bytes).  `lead` is the offset of the
+// first source byte in its block (a multiple of the element size), so stage
+// byte lead + b holds source byte b.  Every staged byte shares a 16-byte
+// block, and so a page, with a valid source byte: the widened read stays in
+// mapped memory, and sources are never written during a call.
+struct Staged {
+  int lead, bytes;
 };
 
-__device__ __forceinline__ Interior interior_of(const char *src, int src_bytes) {
-  const int lead = (int)((16u - ((uint32_t)(uintptr_t)src & 15u)) & 15u);
-  Interior in;
-  in.lo = lead < src_bytes ? lead : src_bytes;
-  in.hi = in.lo + ((src_bytes - in.lo) & ~15);
-  return in;
+__device__ __forceinline__ Staged staged_of(const char *src, int src_bytes) {
+  Staged st;
+  st.lead = (int)((uint32_t)(uintptr_t)src & 15u);
+  st.bytes = src_bytes > 0 ? (st.lead + src_bytes + 15) & ~15 : 0;
+  return st;
 }
 
 // What the producer tells the consumers about the item in a stage: written to
@@ -287,7 +292,7 @@ constexpr int kHeaderBytes = 64;
 static_assert(sizeof(StageHeader) <= kHeaderBytes, "stage header too large");
 constexpr int32_t kSkipItem = -1;
 
-// Consumer side of one item.  `stage` holds the item's staged interior.
+// Consumer side of one item.  `stage` holds the item's staged source.
 // `ct` is the consumer thread index in [0, kConsumers).  Each thread handles
 // kBatch destination vectors per round: it reads all their source words from
 // shared memory first, then converts and stores them.
@@ -300,34 +305,29 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
   using D = typename Traits<KIND>::D;
   constexpr int DU = 16 / (int)sizeof(D);      // elements per destination vector
   constexpr int SW = DU * (int)sizeof(S) / 4;  // source words per vector (2, 4 or 8)
-  constexpr int SB = DU * (int)sizeof(S);      // source bytes per vector
-  const Interior in = interior_of(src, n_copy * (int)sizeof(S));
+  const int lead = (int)((uint32_t)(uintptr_t)src & 15u);
 
   // Destination: scalar head to the first 16-byte boundary, vectors, tail.
   int h = (int)(((16u - ((uint32_t)(uintptr_t)dst & 15u)) & 15u) / sizeof(D));
   h = h < n_total ? h : n_total;
   const int nvec = (n_total - h) / DU;
   const int tail0 = h + nvec * DU;
-  if (ct < h) scalar_elem<KIND>(src, dst, ct, n_copy);
-  if (tail0 + ct < n_total) scalar_elem<KIND>(src, dst, tail0 + ct, n_copy);
+  if (ct < h) scalar_elem<KIND>(stage, lead, dst, ct, n_copy);
+  if (tail0 + ct < n_total) scalar_elem<KIND>(stage, lead, dst, tail0 + ct, n_copy);
 
-  // Every vector's source starts at the same byte phase inside the stage.
-  const int rb = ((h * (int)sizeof(S) - in.lo) & 3) * 8;
+  // Every vector's source starts at the same byte phase inside a stage word.
+  const int rb = ((lead + h * (int)sizeof(S)) & 3) * 8;
   const uint32_t *stage32 = reinterpret_cast<const uint32_t *>(stage);
   for (int base = ct; base < nvec; base += kBatch * kConsumers) {
     uint32_t wv[kBatch][SW + 1];
-    int mode[kBatch];  // 0 none, 1 staged vector, 2 all padding, 3 element by element
+    int mode[kBatch];  // 0 none, 1 whole vector, 2 all padding, 3 element by element (valid then padding)
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int j = base + b * kConsumers;
       const int e0 = h + j * DU;
-      const int s_lo = e0 * (int)sizeof(S);
-      mode[b] = j >= nvec ? 0
-                : e0 >= n_copy ? 2
-                : (e0 + DU <= n_copy && s_lo >= in.lo && s_lo + SB <= in.hi) ? 1
-                                                                               : 3;
+      mode[b] = j >= nvec ? 0 : e0 >= n_copy ? 2 : e0 + DU <= n_copy ? 1 : 3;
       if (mode[b] == 1) {
-        const int wi = (s_lo - in.lo) >> 2;
+        const int wi = (lead + e0 * (int)sizeof(S)) >> 2;
 #pragma unroll
         for (int k = 0; k <= SW; ++k) wv[b][k] = stage32[wi + k];
       }
@@ -358,7 +358,7 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
         store_vec(d, 0u, 0u, 0u, 0u);
       } else if (mode[b] == 3) {
 #pragma unroll 1
-        for (int e = 0; e < DU; ++e) scalar_elem<KIND>(src, dst, e0 + e, n_copy);
+        for (int e = 0; e < DU; ++e) scalar_elem<KIND>(stage, lead, dst, e0 + e, n_copy);
       }
     }
   }
@@ -407,21 +407,21 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       }
       const int ss = (w.kind & 1) ? 2 : 4, ds = (w.kind & 2) ? 2 : 4;
       const char *src = reinterpret_cast<const char *>(a.slot[base + w.src_slot]) + w.src_off * (int64_t)ss;
-      const Interior in = interior_of(src, w.n_copy * ss);
-      uint32_t bytes = (uint32_t)(in.hi - in.lo);
+      const Staged st = staged_of(src, w.n_copy * ss);
+      uint32_t bytes = (uint32_t)st.bytes;
       StageHeader *hd = reinterpret_cast<StageHeader *>(smem + s * kStageStride);
       hd->src = src;
       hd->dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[base + w.dst_slot])) + w.dst_off * (int64_t)ds;
       hd->n_copy = w.n_copy;
       hd->n_total = w.n_total;
       hd->kind = w.kind;
-      if (bytes > (uint32_t)kStageBytes) {  // never planned; the consumers skip it
+      if (bytes > (uint32_t)kStagedMax) {  // never planned; the consumers skip it
         atomicOr(a.status, kStatusBadItem);
         hd->kind = kSkipItem;
         bytes = 0;
       }
       mbar_arrive_expect_tx(&full[s], bytes);
-      if (bytes) bulk_copy_g2s(smem + s * kStageStride + kHeaderBytes, src + in.lo, bytes, &full[s]);
+      if (bytes) bulk_copy_g2s(smem + s * kStageStride + kHeaderBytes, src - st.lead, bytes, &full[s]);
     }
     // Leave no bulk copy in flight when this thread exits: wait for the last
     // armed phase of every stage (consumers may have left early).
