@@ -56,12 +56,16 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kStages = 4;
-// Each stage holds a 64-byte header (the item, see StageHeader) and the
-// item's staged source: its source bytes widened to whole aligned 16-byte
-// blocks, at most kStageBytes + 16 bytes.  The funnel read of the last vector
-// may touch one word past them, hence 32 bytes of slack in all.
+// Each stage holds the item's staged source -- its source bytes widened to
+// whole aligned 16-byte blocks, at most kStageBytes + 16 bytes, plus slack
+// for the funnel read of the last vector, which may touch one word past them
+// -- and after it a 64-byte header (the item, see StageHeader).  Stages start
+// on 128-byte boundaries, where the bulk copies write them.
 constexpr int kStagedMax = (int)kStageBytes + 16;
-constexpr int kStageStride = 64 + (int)kStageBytes + 32;
+constexpr int kStageDataBytes = (int)kStageBytes + 32;
+constexpr int kHeaderBytes = 64;
+constexpr int kStageStride = (kStageDataBytes + kHeaderBytes + 127) / 128 * 128;
+static_assert(kStageDataBytes % 16 == 0, "stage header must stay 16-byte aligned");
 constexpr int kSmemBytes = kStages * kStageStride + 2 * kStages * 8;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -288,7 +292,6 @@ struct StageHeader {
   int32_t kind;     // kSkipItem: nothing to do (refused by the producer)
   int32_t reserved;
 };
-constexpr int kHeaderBytes = 64;
 static_assert(sizeof(StageHeader) <= kHeaderBytes, "stage header too large");
 constexpr int32_t kSkipItem = -1;
 
@@ -315,8 +318,13 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
   if (ct < h) scalar_elem<KIND>(stage, lead, dst, ct, n_copy);
   if (tail0 + ct < n_total) scalar_elem<KIND>(stage, lead, dst, tail0 + ct, n_copy);
 
-  // Every vector's source starts at the same byte phase inside a stage word.
+  // Every vector's source starts at the same byte phase inside a stage word
+  // (vectors are SW words apart).  When that phase is zero and the first
+  // vector's word is aligned to the load width, every vector's source is SW
+  // whole words read with 8- or 16-byte loads and no shift ("wide").
   const int rb = ((lead + h * (int)sizeof(S)) & 3) * 8;
+  constexpr int WA = SW < 4 ? SW : 4;  // words per wide load
+  const bool wide = rb == 0 && (((lead + h * (int)sizeof(S)) >> 2) % WA) == 0;
   const uint32_t *stage32 = reinterpret_cast<const uint32_t *>(stage);
   for (int base = ct; base < nvec; base += kBatch * kConsumers) {
     uint32_t wv[kBatch][SW + 1];
@@ -328,8 +336,26 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
       mode[b] = j >= nvec ? 0 : e0 >= n_copy ? 2 : e0 + DU <= n_copy ? 1 : 3;
       if (mode[b] == 1) {
         const int wi = (lead + e0 * (int)sizeof(S)) >> 2;
+        if (wide) {
+          if constexpr (SW == 2) {
+            const uint2 t = *reinterpret_cast<const uint2 *>(stage32 + wi);
+            wv[b][0] = t.x;
+            wv[b][1] = t.y;
+          } else {
 #pragma unroll
-        for (int k = 0; k <= SW; ++k) wv[b][k] = stage32[wi + k];
+            for (int q = 0; q < SW / 4; ++q) {
+              const uint4 t = *reinterpret_cast<const uint4 *>(stage32 + wi + 4 * q);
+              wv[b][4 * q + 0] = t.x;
+              wv[b][4 * q + 1] = t.y;
+              wv[b][4 * q + 2] = t.z;
+              wv[b][4 * q + 3] = t.w;
+            }
+          }
+          wv[b][SW] = 0;
+        } else {
+#pragma unroll
+          for (int k = 0; k <= SW; ++k) wv[b][k] = stage32[wi + k];
+        }
       }
     }
 #pragma unroll
@@ -339,7 +365,7 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
       if (mode[b] == 1) {
         uint32_t sw[SW];
 #pragma unroll
-        for (int k = 0; k < SW; ++k) sw[k] = __funnelshift_r(wv[b][k], wv[b][k + 1], rb);
+        for (int k = 0; k < SW; ++k) sw[k] = wide ? wv[b][k] : __funnelshift_r(wv[b][k], wv[b][k + 1], rb);
         uint32_t o[4];
         if constexpr (KIND == KIND_BF16_F32) {
           o[0] = sw[0] << 16;
@@ -409,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       const char *src = reinterpret_cast<const char *>(a.slot[base + w.src_slot]) + w.src_off * (int64_t)ss;
       const Staged st = staged_of(src, w.n_copy * ss);
       uint32_t bytes = (uint32_t)st.bytes;
-      StageHeader *hd = reinterpret_cast<StageHeader *>(smem + s * kStageStride);
+      StageHeader *hd = reinterpret_cast<StageHeader *>(smem + s * kStageStride + kStageDataBytes);
       hd->src = src;
       hd->dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[base + w.dst_slot])) + w.dst_off * (int64_t)ds;
       hd->n_copy = w.n_copy;
@@ -421,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         bytes = 0;
       }
       mbar_arrive_expect_tx(&full[s], bytes);
-      if (bytes) bulk_copy_g2s(smem + s * kStageStride + kHeaderBytes, src - st.lead, bytes, &full[s]);
+      if (bytes) bulk_copy_g2s(smem + s * kStageStride, src - st.lead, bytes, &full[s]);
     }
     // Leave no bulk copy in flight when this thread exits: wait for the last
     // armed phase of every stage (consumers may have left early).
@@ -443,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
       return;
     }
-    const StageHeader hd = *reinterpret_cast<const StageHeader *>(smem + s * kStageStride);
-    const uint8_t *stage = smem + s * kStageStride + kHeaderBytes;
+    const StageHeader hd = *reinterpret_cast<const StageHeader *>(smem + s * kStageStride + kStageDataBytes);
+    const uint8_t *stage = smem + s * kStageStride;
     switch (hd.kind) {
       case KIND_F32_F32: consume_item<KIND_F32_F32>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
       case KIND_BF16_F32: consume_item<KIND_BF16_F32>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
