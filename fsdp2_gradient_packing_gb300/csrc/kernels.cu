@@ -720,9 +720,11 @@ fsdp_status_t check_ptr(const void *p, int64_t bytes, int64_t align, const char 
   return FSDP_OK;
 }
 
-template <int NSLOT>
+// Every walk_kernel instance may use kSmemBytes of dynamic shared memory
+// (needed once that is above the 48 KB default).
+template <class Args>
 cudaError_t allow_smem() {
-  return cudaFuncSetAttribute(reinterpret_cast<const void *>(&walk_kernel<LaunchArgs<NSLOT>>),
+  return cudaFuncSetAttribute(reinterpret_cast<const void *>(&walk_kernel<Args>),
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
@@ -762,6 +764,9 @@ void noalloc_setup(NoAllocDevice &nd, int dev) {
   void *ptr = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = allow_smem<LaunchArgs<kSlotsSmall>>();
+  if (e == cudaSuccess) e = allow_smem<LaunchArgs<kSlotsMedium>>();
+  if (e == cudaSuccess) e = allow_smem<LaunchArgs<kSlotsLarge>>();
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<LaunchArgs<kSlotsSmall>>, kThreads, kSmemBytes);
   nd.err = e;
@@ -806,9 +811,12 @@ fsdp_status_t device_setup(fsdp_layout *L) {
   int dev = -1, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = allow_smem<kSlotsSmall>();
-  if (e == cudaSuccess) e = allow_smem<kSlotsMedium>();
-  if (e == cudaSuccess) e = allow_smem<kSlotsLarge>();
+  if (e == cudaSuccess) e = allow_smem<LaunchArgs<kSlotsSmall>>();
+  if (e == cudaSuccess) e = allow_smem<LaunchArgs<kSlotsMedium>>();
+  if (e == cudaSuccess) e = allow_smem<LaunchArgs<kSlotsLarge>>();
+  if (e == cudaSuccess) e = allow_smem<BatchArgs<kSlotsSmall>>();
+  if (e == cudaSuccess) e = allow_smem<BatchArgs<kSlotsMedium>>();
+  if (e == cudaSuccess) e = allow_smem<BatchArgs<kBatchSlotsLarge>>();
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, walk_kernel<LaunchArgs<kSlotsSmall>>, kThreads, kSmemBytes);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("device query failed: ") + cudaGetErrorString(e));
