@@ -45,7 +45,7 @@ static_assert(sizeof(WorkItem) == 32, "work item must stay 32 bytes");
 // shared-memory stage of the kernel's pipeline, so they may not exceed
 // kStageBytes; its destination bytes are bounded too so that long runs split
 // into pieces that balance across the grid.
-constexpr int64_t kStageBytes = 8 * 1024;
+constexpr int64_t kStageBytes = 16 * 1024;
 constexpr int64_t kItemDstBytes = 16 * 1024;
 
 enum Op { OP_PACK = 0, OP_COPY_IN = 1, OP_COPY_OUT = 2, OP_RS_COPY_OUT = 3, OP_COUNT = 4 };

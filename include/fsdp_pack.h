@@ -331,7 +331,7 @@ fsdp_status_t fsdp_reduce_scatter_copy_out_batched(const fsdp_layout_t *const *l
  *   L:  a layout from fsdp_plan_layout_host (planned without any CUDA call) or
  *       from fsdp_plan_layout; its pack table may hold at most 131,064 work
  *       items, else FSDP_EUNSUPPORTED and nothing is launched.  (The 50.3M
- *       element group at W = 8 needs 12,352; items are runs of at most 8 KiB
+ *       element group at W = 8 needs 12,352; items are runs of at most 16 KiB
  *       of source and 16 KiB of destination.)
  *   grads, bucket_bufs, stream: as for fsdp_pack_reduce_scatter.
  * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call

@@ -122,7 +122,7 @@ def test_empty_layout(fp):
 
 def test_work_items_cover_the_buffers(fp):
     # Pack items are (rank, parameter) runs cut to at most 16 KiB of
-    # destination and 8 KiB of source: the counts follow from the run lengths.
+    # destination and 16 KiB of source: the counts follow from the run lengths.
     work = wl.mixed_50m()
     with fp.fsdp_plan_layout_host(work.groups[0], 8) as L:
         info = fp.fsdp_layout_query(L)
