@@ -35,7 +35,6 @@ destination slot including padding and alignment gaps):
 from __future__ import annotations
 
 import argparse
-import ctypes
 import hashlib
 import json
 import math
