@@ -243,6 +243,45 @@ def test_emulated_rs_bf16_rounding_on_every_first_operand(fp, phase):
     assert np.array_equal(got, want), first_mismatch(got, want)
 
 
+@pytest.mark.parametrize("phase", [0, 2])
+def test_emulated_rs_at_the_rank_limit(fp, phase):
+    """256 ranks, the limit: every element is the rank-ordered sum of 256
+    inputs, in an FP32 and a BF16 bucket with special values, against the
+    oracle (phase 2 on one input takes the element path).  257 ranks are
+    refused before anything is launched."""
+    specs = [wl.ParamSpec("a", (1000,), "f32", "f32", "f32", "f32"),
+             wl.ParamSpec("b", (700,), "bf16", "bf16", "f32", "bf16")]
+    for W in (256, 257):
+        pl = oracle.plan(oracle.params_from_specs(specs), W)
+        names = ["f32" if d == oracle.F32 else "bf16" for d in pl.bucket_dtype]
+        packed = []
+        for q in range(W):
+            row = []
+            for b, (name, S) in enumerate(zip(names, pl.bucket_S)):
+                bits = wl.normal_bits(W * S, name, 1.0, 7200, q, b)
+                wl.inject_specials(bits, name, 0.002, 7200, q, b)
+                row.append(bits)
+            packed.append(row)
+        with fp.fsdp_plan_layout(specs, W) as L:
+            ins = [DevBuf(packed[q][b].nbytes, phase if (q == 1 and b == 1) else 0, packed[q][b])
+                   for b in range(len(names)) for q in range(W)]
+            outs = [DevBuf(W * S * ESZ[name]) for name, S in zip(names, pl.bucket_S)]
+            if W > 256:
+                with pytest.raises(fp.FsdpError) as e:
+                    fp.fsdp_emulated_reduce_scatter(L, [x.ptr for x in ins], [o.ptr for o in outs])
+                assert e.value.status == fp.FSDP_EUNSUPPORTED
+                torch.cuda.synchronize()
+                assert all(bool((o.raw == 0xA5).all()) for o in outs)
+                continue
+            fp.fsdp_emulated_reduce_scatter(L, [x.ptr for x in ins], [o.ptr for o in outs])
+            fp.fsdp_sync_status(L)
+            want = oracle.emulated_reduce_scatter(pl, packed)
+            for b, (o, name) in enumerate(zip(outs, names)):
+                got = o.read(NP[name])
+                assert o.guards_ok()
+                assert np.array_equal(got, want[b]), f"bucket {b}: {first_mismatch(got, want[b])}"
+
+
 def test_batched_transformer500_all_layers_in_one_launch(fp):
     work = wl.transformer_500(W=8)
     runs = [GroupRun(fp, specs, work.W, work, g) for g, specs in enumerate(work.groups)]
