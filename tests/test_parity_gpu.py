@@ -307,6 +307,46 @@ def test_batched_random_layouts_mixed_world_sizes(fp, batch):
             run.close()
 
 
+def _many_params_workload(seed: int, n: int, W: int = 4) -> wl.Workload:
+    """n small parameters of random length and dtypes, one group, reduce FP32."""
+    rnd = np.random.default_rng(seed)
+    dts = ["f32", "bf16"]
+    specs = tuple(wl.ParamSpec(f"p{i}", (int(rnd.integers(1, 40)),), dts[int(rnd.integers(0, 2))], "f32", "f32",
+                               dts[int(rnd.integers(0, 2))]) for i in range(n))
+    return wl.Workload(f"many{seed}", W, (specs,), 1.0, seed)
+
+
+def test_batched_at_the_layout_and_pointer_limits(fp):
+    """64 layouts in one batched call (the limit), and two layouts of 1,919
+    parameters whose calls pass exactly 3,840 pointers (the largest parameter
+    block), each against the oracle; one pointer more is refused before
+    anything is launched."""
+    for works in ([wl.random_layout(4100 + k, max_params=4, max_numel=3000) for k in range(64)],
+                  [_many_params_workload(7300 + k, 1919) for k in range(2)]):
+        runs = []
+        try:
+            for k, work in enumerate(works):
+                runs.append(GroupRun(fp, work.groups[0], work.W, work, 0, misalign_seed=5000 + k, specials=0.02))
+            assert_batched_parity(fp, runs)
+        finally:
+            for run in runs:
+                run.close()
+    works = [_many_params_workload(7400 + k, 1920) for k in range(2)]
+    layouts = [fp.fsdp_plan_layout(w.groups[0], w.W) for w in works]
+    try:
+        mem = DevBuf(1 << 20)            # every pointer below points into it
+        grads = [mem.ptr + 256 * i for i in range(2 * 1920)]
+        buckets = [mem.ptr + (1 << 19), mem.ptr + (3 << 18)]
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_pack_reduce_scatter_batched(layouts, grads, buckets)
+        assert e.value.status == fp.FSDP_EUNSUPPORTED
+        torch.cuda.synchronize()
+        assert bool((mem.raw == 0xA5).all())
+    finally:
+        for L in layouts:
+            L.close()
+
+
 def test_batched_with_empty_layouts(fp):
     works = [wl.Workload("e0", 4, ((),), seed=1),
              wl.tiny_two_blocks(W=4, grouping="model"),
