@@ -496,6 +496,65 @@ def test_torch_tensors_of_the_layout_dtypes_are_accepted_and_checked(fp):
             assert np.array_equal(got, w), first_mismatch(got, w)
 
 
+def test_flow_around_torch_collectives(fp):
+    """The README's flow on a one-rank NCCL process group (the collectives are
+    then copies): pack, reduce_scatter_tensor, reduce-scatter copy-out;
+    copy-in, all_gather_into_tensor, copy-out; every output against the oracle."""
+    import socket
+    import torch.distributed as dist
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        W = dist.get_world_size()
+        F32, BF16 = fp.FSDP_DTYPE_F32, fp.FSDP_DTYPE_BF16
+        specs = [wl.ParamSpec("w", (1024, 1024), "bf16", "f32", "f32", "bf16"),
+                 wl.ParamSpec("n", (1024,), "f32", "f32", "f32", "f32")]
+        work = wl.Workload("flow", W, (tuple(specs),), 1.0, 7500)
+        params = [(s.numel, fp.DTYPE_CODES[s.grad_dtype], fp.DTYPE_CODES[s.reduce_dtype],
+                   fp.DTYPE_CODES[s.shard_dtype], fp.DTYPE_CODES[s.param_dtype]) for s in specs]
+        tdt = {F32: torch.float32, BF16: torch.bfloat16}
+        ncode = {"f32": F32, "bf16": BF16}
+        ibits = {F32: torch.int32, BF16: torch.int16}
+        pl = oracle.plan(oracle.params_from_specs(specs), W)
+        grads_np = [wl.grad_values(work, 0, i) for i in range(len(specs))]
+        shards_np = [wl.shard_values(work, 0, i, 0, c, min(c, s.numel)) for i, (s, c) in enumerate(zip(specs, pl.chunk))]
+        to_dev = lambda x, code: torch.from_numpy(x.view(np.int32 if code == F32 else np.int16).copy()).cuda().view(tdt[code])
+        with fp.fsdp_plan_layout(params, W) as L:
+            info = fp.fsdp_layout_query(L)
+            buckets = [fp.fsdp_layout_bucket(L, b) for b in range(info.n_buckets)]
+            chunk = [fp.fsdp_layout_param(L, p).chunk for p in range(info.n_params)]
+            grads = [to_dev(g, ncode[s.grad_dtype]) for g, s in zip(grads_np, specs)]
+            bufs = [torch.empty(W * b.row_elems, dtype=tdt[b.reduce_dtype], device="cuda") for b in buckets]
+            fp.fsdp_pack_reduce_scatter(L, grads, bufs)
+            rows = [torch.empty(b.row_elems, dtype=tdt[b.reduce_dtype], device="cuda") for b in buckets]
+            for buf, row in zip(bufs, rows):
+                dist.reduce_scatter_tensor(row, buf)
+            sharded = [torch.empty(c, dtype=tdt[ncode[s.shard_dtype]], device="cuda") for s, c in zip(specs, chunk)]
+            fp.fsdp_reduce_scatter_copy_out(L, rows, sharded)
+            shards = [to_dev(x, ncode[s.shard_dtype]) for x, s in zip(shards_np, specs)]
+            ag_in = torch.empty(info.ag_bytes, dtype=torch.uint8, device="cuda")
+            fp.fsdp_allgather_copy_in(L, shards, ag_in)
+            ag_out = torch.empty(W * info.ag_bytes, dtype=torch.uint8, device="cuda")
+            dist.all_gather_into_tensor(ag_out, ag_in)
+            full = [torch.empty(s.numel, dtype=tdt[ncode[s.param_dtype]], device="cuda") for s in specs]
+            fp.fsdp_allgather_copy_out(L, ag_out, full)
+            fp.fsdp_sync_status(L)
+        bits = lambda t, code: t.view(ibits[code]).cpu().numpy().view(np.uint32 if code == F32 else np.uint16)
+        want_b = oracle.pack_reduce_scatter(pl, grads_np)
+        for t, w, b in zip(bufs, want_b, buckets):
+            assert np.array_equal(bits(t, b.reduce_dtype), w)
+        for t, w, s in zip(sharded, oracle.reduce_scatter_copy_out(pl, want_b), specs):
+            assert np.array_equal(bits(t, ncode[s.shard_dtype]), w)
+        want_row = oracle.allgather_copy_in(pl, shards_np)
+        assert np.array_equal(ag_out.cpu().numpy(), want_row)
+        for t, w, s in zip(full, oracle.allgather_copy_out(pl, want_row), specs):
+            assert np.array_equal(bits(t, ncode[s.param_dtype]), w)
+    finally:
+        dist.destroy_process_group()
+
+
 def test_empty_layout_and_empty_parameters(fp):
     with fp.fsdp_plan_layout([], 8) as L:
         fp.fsdp_pack_reduce_scatter(L, [], [])
