@@ -56,9 +56,9 @@ from fsdp2_gradient_packing_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "reduce-scatter pack GB/s and ms per fully_shard (50.3M elem, W=8) vs HBM peak"
 UNIT = "GB/s"
-NOMINAL_HBM_GBS = 8000.0
-CHUNKING = {False: "flattened: c_p = ceil(n_p / W)", True: "dim-0 rows: c_p = ceil(d0 / W) * row elements"}   # the "~8 TB/s" HBM figure the metric is quoted against
-FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the metric is quoted against
+FALLBACK_HBM_GBS = 6800.0  # used only when no measured copy bandwidth is available
+CHUNKING = {False: "flattened: c_p = ceil(n_p / W)", True: "dim-0 rows: c_p = ceil(d0 / W) * row elements"}
 ESZ = {"f32": 4, "bf16": 2}
 STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
 STEP_RS = " + reduce-scatter copy-out (row 0 of each bucket as this rank's reduced row)"
