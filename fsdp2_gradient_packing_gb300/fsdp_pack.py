@@ -265,66 +265,129 @@ def _layout_slots(layout: Layout) -> dict:
     return layout._slots
 
 
-def _torch_dtype_code(t):
-    import torch
-    return {torch.float32: FSDP_DTYPE_F32, torch.bfloat16: FSDP_DTYPE_BF16}.get(t.dtype, "other")
+_FLOAT_CODES = None
+_TENSOR_TYPE = [None]
 
 
-def _check_args(where: str, what: str, ts, slots, device, placement: bool) -> None:
-    """Raise ValueError if ``ts`` (a list, a tensor or int for a single slot,
-    or a prebuilt pointer array) does not fit ``slots``: counts, sizes,
-    dtypes and contiguity, or with ``placement`` the tensors' devices."""
+def _float_codes() -> dict:
+    """torch float dtype -> FSDP dtype code (built on first use, with the
+    tensor type the checks recognise)."""
+    global _FLOAT_CODES
+    if _FLOAT_CODES is None:
+        import torch
+        _TENSOR_TYPE[0] = torch.Tensor
+        _FLOAT_CODES = {torch.float32: FSDP_DTYPE_F32, torch.bfloat16: FSDP_DTYPE_BF16}
+    return _FLOAT_CODES
+
+
+def _dtype_name(dt: int) -> str:
+    return "f32" if dt == FSDP_DTYPE_F32 else "bf16"
+
+
+def _slot_name(what: str, k: int, single: bool) -> str:
+    return what if single else f"{what}[{k}]"
+
+
+def _scan_args(where: str, what: str, ts, slots, device):
+    """Check ``ts`` (a list, a tensor or int for a single slot, or a prebuilt
+    pointer array) against ``slots`` in one pass, gathering its pointers as it
+    goes.  Returns (error, placement error, value for the C call): the first
+    count, size, dtype or contiguity error and the first device error, each a
+    message or None, and the pointer array or pointer to pass."""
     if ts is None or isinstance(ts, int):
-        return
+        return None, None, ts
     if isinstance(ts, ctypes.Array):
         if len(slots) > len(ts):
-            raise ValueError(f"{where}: {what} holds {len(ts)} pointers, the layout needs {len(slots)}")
-        return
+            return f"{where}: {what} holds {len(ts)} pointers, the layout needs {len(slots)}", None, None
+        return None, None, ts
     single = not isinstance(ts, (list, tuple))
-    items = [ts] if single else list(ts)
+    items = (ts,) if single else ts
     if len(items) != len(slots):
-        raise ValueError(f"{where}: {len(items)} {what} given, the layout has {len(slots)}")
-    for k, (t, (need, dt)) in enumerate(zip(items, slots)):
-        if t is None or isinstance(t, int) or not hasattr(t, "data_ptr"):
+        return f"{where}: {len(items)} {what} given, the layout has {len(slots)}", None, None
+    codes, tensor_type = _float_codes(), _TENSOR_TYPE[0]
+    placement = None
+    ptrs = []
+    for k, t in enumerate(items):
+        if not isinstance(t, tensor_type):
+            ptrs.append(t)  # an int or None; anything else is refused by ctypes
             continue
-        name = what if single else f"{what}[{k}]"
-        if placement:
-            if need and not t.is_cuda:
-                raise ValueError(f"{where}: {name} is not a CUDA tensor")
-            if need and device is not None and t.device.index != device:
-                raise ValueError(f"{where}: {name} is on cuda:{t.device.index}, the layout on cuda:{device}")
-            continue
+        need, dt = slots[k]
         if not t.is_contiguous():
-            raise ValueError(f"{where}: {name} is not contiguous")
-        have = t.numel() * t.element_size()
+            return f"{where}: {_slot_name(what, k, single)} is not contiguous", None, None
+        have = t.nbytes
         if have < need:
-            raise ValueError(f"{where}: {name} holds {have} bytes, the layout needs {need}")
-        if dt is not None and t.is_floating_point() and _torch_dtype_code(t) != dt:
-            raise ValueError(f"{where}: {name} is {t.dtype}, the layout's dtype is "
-                             f"{'f32' if dt == FSDP_DTYPE_F32 else 'bf16'} (pass raw bits as an integer tensor)")
+            return f"{where}: {_slot_name(what, k, single)} holds {have} bytes, the layout needs {need}", None, None
+        if dt is not None:
+            tdt = t.dtype
+            code = codes.get(tdt)
+            if code != dt and (code is not None or tdt.is_floating_point):
+                return (f"{where}: {_slot_name(what, k, single)} is {tdt}, the layout's dtype is "
+                        f"{_dtype_name(dt)} (pass raw bits as an integer tensor)"), None, None
+        if placement is None and need:
+            index = t.get_device()  # -1 off the GPU
+            if index < 0:
+                placement = f"{where}: {_slot_name(what, k, single)} is not a CUDA tensor"
+            elif device is not None and index != device:
+                placement = (f"{where}: {_slot_name(what, k, single)} is on cuda:{index}, "
+                             f"the layout on cuda:{device}")
+        ptrs.append(t.data_ptr())
+    if single:
+        return None, placement, ptrs[0]
+    return None, placement, (_P * max(1, len(ptrs)))(*ptrs)
 
 
-def _check_lists(where: str, slots: dict, lists: dict) -> None:
-    for placement in (False, True):  # every count, size and dtype first, then devices
-        for what, ts in lists.items():
-            _check_args(where, what, ts, slots.get(what, []), slots["device"], placement)
+def _check_lists(where: str, slots: dict, lists: dict) -> list:
+    """Raise ValueError for the first count, size, dtype or contiguity error
+    of any list (in list order); only if there is none, for the first device
+    error.  Returns the lists' values for the C call, in order."""
+    device = slots["device"]
+    placement = None
+    values = []
+    for what, ts in lists.items():
+        err, perr, value = _scan_args(where, what, ts, slots.get(what, []), device)
+        if err is not None:
+            raise ValueError(err)
+        if placement is None:
+            placement = perr
+        values.append(value)
+    if placement is not None:
+        raise ValueError(placement)
+    return values
 
 
-def _check_layout_args(where: str, layout: Layout, **lists) -> None:
+def _as_list(ts):
+    """A per-layout argument of a batched call as a list (a lone tensor or
+    pointer stands for a batch of one)."""
+    return ts if isinstance(ts, (list, tuple, ctypes.Array)) else [ts]
+
+
+def _marshal(ts):
+    """The value for the C call without checks: a prebuilt array as is, a
+    list as a pointer array, a single tensor or int as its pointer."""
+    if isinstance(ts, ctypes.Array):
+        return ts
+    if isinstance(ts, (list, tuple)):
+        return pointer_array(ts)
+    return _ptr(ts)
+
+
+def _layout_args(where: str, layout: Layout, **lists) -> list:
+    """Check the lists against one layout and return them marshalled."""
     if not isinstance(layout, Layout) or not layout.handle:
-        return  # the C call reports a null or closed layout
-    _check_lists(where, _layout_slots(layout), lists)
+        return [_marshal(ts) for ts in lists.values()]  # the C call reports a null or closed layout
+    return _check_lists(where, _layout_slots(layout), lists)
 
 
-def _check_batched_args(where: str, la: "LayoutArray", **lists) -> None:
+def _batched_args(where: str, la: "LayoutArray", **lists) -> list:
+    """Check the concatenated lists against a layout array and return them marshalled."""
     if not all(isinstance(L, Layout) and L.handle for L in la.layouts):
-        return  # the C call reports a null or closed layout
+        return [_marshal(ts) for ts in lists.values()]  # the C call reports a null or closed layout
     if la.slots is None:  # the layouts' slot lists concatenated, once per array
         per = [_layout_slots(L) for L in la.layouts]
         devices = {s["device"] for s in per}
         la.slots = {k: [x for s in per for x in s[k]] for k in per[0] if k != "device"} if per else {}
         la.slots["device"] = devices.pop() if len(devices) == 1 else None
-    _check_lists(where, la.slots, lists)
+    return _check_lists(where, la.slots, lists)
 
 
 def _ptr(t) -> int | None:
@@ -340,51 +403,65 @@ def pointer_array(ts):
     of a list to skip re-marshalling on every call."""
     if isinstance(ts, ctypes.Array):
         return ts
-    arr = (_P * max(1, len(ts)))()
-    for k, t in enumerate(ts):
-        arr[k] = _ptr(t)
-    return arr
+    if not ts:
+        return (_P * 1)()
+    return (_P * len(ts))(*[t if t is None or isinstance(t, int) else t.data_ptr() for t in ts])
+
+
+_current_stream_fn = None
+
+
+def _current_stream() -> int:
+    """torch's current CUDA stream on the current device, as a handle.  The
+    first call takes it through torch.cuda (which initialises CUDA); later
+    calls read the raw handle directly when this torch build exposes it and
+    it agreed with torch.cuda on that first call."""
+    global _current_stream_fn
+    if _current_stream_fn is None:
+        import torch
+        public = torch.cuda.current_stream().cuda_stream
+        raw, dev = getattr(torch._C, "_cuda_getCurrentRawStream", None), getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and dev is not None and raw(dev()) == public:
+            _current_stream_fn = lambda: raw(dev())  # noqa: E731
+        else:
+            _current_stream_fn = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
+        return public
+    return _current_stream_fn()
 
 
 def _stream(stream) -> int | None:
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
 
 
 def fsdp_pack_reduce_scatter(layout: Layout, grads, bucket_bufs, stream=None) -> None:
-    _check_layout_args("fsdp_pack_reduce_scatter", layout, grads=grads, buckets=bucket_bufs)
-    _check(_lib.fsdp_pack_reduce_scatter(layout.handle, pointer_array(grads), pointer_array(bucket_bufs),
-                                         _stream(stream)), "fsdp_pack_reduce_scatter")
+    g, b = _layout_args("fsdp_pack_reduce_scatter", layout, grads=grads, buckets=bucket_bufs)
+    _check(_lib.fsdp_pack_reduce_scatter(layout.handle, g, b, _stream(stream)), "fsdp_pack_reduce_scatter")
 
 
 def fsdp_allgather_copy_in(layout: Layout, local_shards, ag_input, stream=None) -> None:
-    _check_layout_args("fsdp_allgather_copy_in", layout, shards=local_shards, ag_input=ag_input)
-    _check(_lib.fsdp_allgather_copy_in(layout.handle, pointer_array(local_shards), _ptr(ag_input),
-                                       _stream(stream)), "fsdp_allgather_copy_in")
+    sh, a = _layout_args("fsdp_allgather_copy_in", layout, shards=local_shards, ag_input=ag_input)
+    _check(_lib.fsdp_allgather_copy_in(layout.handle, sh, a, _stream(stream)), "fsdp_allgather_copy_in")
 
 
 def fsdp_allgather_copy_out(layout: Layout, ag_output, full_params, stream=None) -> None:
-    _check_layout_args("fsdp_allgather_copy_out", layout, ag_output=ag_output, full=full_params)
-    _check(_lib.fsdp_allgather_copy_out(layout.handle, _ptr(ag_output), pointer_array(full_params),
-                                        _stream(stream)), "fsdp_allgather_copy_out")
+    a, f = _layout_args("fsdp_allgather_copy_out", layout, ag_output=ag_output, full=full_params)
+    _check(_lib.fsdp_allgather_copy_out(layout.handle, a, f, _stream(stream)), "fsdp_allgather_copy_out")
 
 
 def fsdp_reduce_scatter_copy_out(layout: Layout, reduced_rows, sharded_grads, stream=None) -> None:
-    _check_layout_args("fsdp_reduce_scatter_copy_out", layout, rows=reduced_rows, sharded=sharded_grads)
-    _check(_lib.fsdp_reduce_scatter_copy_out(layout.handle, pointer_array(reduced_rows), pointer_array(sharded_grads),
-                                             _stream(stream)), "fsdp_reduce_scatter_copy_out")
+    r, sg = _layout_args("fsdp_reduce_scatter_copy_out", layout, rows=reduced_rows, sharded=sharded_grads)
+    _check(_lib.fsdp_reduce_scatter_copy_out(layout.handle, r, sg, _stream(stream)), "fsdp_reduce_scatter_copy_out")
 
 
 def fsdp_emulated_reduce_scatter(layout: Layout, packed, reduced, stream=None) -> None:
     """packed: n_buckets * W pointers, bucket-major (packed[b*W + q] = rank q's
     bucket b); reduced: one [W, S_b] buffer per bucket."""
-    _check_layout_args("fsdp_emulated_reduce_scatter", layout, packed=packed, reduced=reduced)
-    _check(_lib.fsdp_emulated_reduce_scatter(layout.handle, pointer_array(packed), pointer_array(reduced),
-                                             _stream(stream)), "fsdp_emulated_reduce_scatter")
+    pk, rd = _layout_args("fsdp_emulated_reduce_scatter", layout, packed=packed, reduced=reduced)
+    _check(_lib.fsdp_emulated_reduce_scatter(layout.handle, pk, rd, _stream(stream)), "fsdp_emulated_reduce_scatter")
 
 
 class LayoutArray:
@@ -407,44 +484,40 @@ def layout_array(layouts) -> LayoutArray:
 def fsdp_pack_reduce_scatter_batched(layouts, grads, bucket_bufs, stream=None) -> None:
     """grads / bucket_bufs: the per-layout lists concatenated in layout order."""
     la = layout_array(layouts)
-    _check_batched_args("fsdp_pack_reduce_scatter_batched", la, grads=grads, buckets=bucket_bufs)
-    _check(_lib.fsdp_pack_reduce_scatter_batched(la.arr, la.n, pointer_array(grads), pointer_array(bucket_bufs),
-                                                 _stream(stream)),
+    g, b = _batched_args("fsdp_pack_reduce_scatter_batched", la, grads=grads, buckets=bucket_bufs)
+    _check(_lib.fsdp_pack_reduce_scatter_batched(la.arr, la.n, g, b, _stream(stream)),
            "fsdp_pack_reduce_scatter_batched")
 
 
 def fsdp_allgather_copy_in_batched(layouts, local_shards, ag_inputs, stream=None) -> None:
     """local_shards concatenated in layout order; one ag_input per layout."""
     la = layout_array(layouts)
-    _check_batched_args("fsdp_allgather_copy_in_batched", la, shards=local_shards, ag_input=ag_inputs)
-    _check(_lib.fsdp_allgather_copy_in_batched(la.arr, la.n, pointer_array(local_shards), pointer_array(ag_inputs),
-                                               _stream(stream)),
+    sh, a = _batched_args("fsdp_allgather_copy_in_batched", la, shards=local_shards, ag_input=_as_list(ag_inputs))
+    _check(_lib.fsdp_allgather_copy_in_batched(la.arr, la.n, sh, a, _stream(stream)),
            "fsdp_allgather_copy_in_batched")
 
 
 def fsdp_allgather_copy_out_batched(layouts, ag_outputs, full_params, stream=None) -> None:
     """One ag_output per layout; full_params concatenated in layout order."""
     la = layout_array(layouts)
-    _check_batched_args("fsdp_allgather_copy_out_batched", la, ag_output=ag_outputs, full=full_params)
-    _check(_lib.fsdp_allgather_copy_out_batched(la.arr, la.n, pointer_array(ag_outputs), pointer_array(full_params),
-                                                _stream(stream)),
+    a, f = _batched_args("fsdp_allgather_copy_out_batched", la, ag_output=_as_list(ag_outputs), full=full_params)
+    _check(_lib.fsdp_allgather_copy_out_batched(la.arr, la.n, a, f, _stream(stream)),
            "fsdp_allgather_copy_out_batched")
 
 
 def fsdp_reduce_scatter_copy_out_batched(layouts, reduced_rows, sharded_grads, stream=None) -> None:
     """reduced_rows / sharded_grads: the per-layout lists concatenated in layout order."""
     la = layout_array(layouts)
-    _check_batched_args("fsdp_reduce_scatter_copy_out_batched", la, rows=reduced_rows, sharded=sharded_grads)
-    _check(_lib.fsdp_reduce_scatter_copy_out_batched(la.arr, la.n, pointer_array(reduced_rows),
-                                                     pointer_array(sharded_grads), _stream(stream)),
+    r, sg = _batched_args("fsdp_reduce_scatter_copy_out_batched", la, rows=reduced_rows, sharded=sharded_grads)
+    _check(_lib.fsdp_reduce_scatter_copy_out_batched(la.arr, la.n, r, sg, _stream(stream)),
            "fsdp_reduce_scatter_copy_out_batched")
 
 
 def fsdp_pack_reduce_scatter_noalloc(layout: Layout, grads, bucket_bufs, stream=None) -> None:
     """The pack with its scratch in the library's static array (no allocation)."""
-    _check_layout_args("fsdp_pack_reduce_scatter_noalloc", layout, grads=grads, buckets=bucket_bufs)
-    _check(_lib.fsdp_pack_reduce_scatter_noalloc(layout.handle, pointer_array(grads), pointer_array(bucket_bufs),
-                                                 _stream(stream)), "fsdp_pack_reduce_scatter_noalloc")
+    g, b = _layout_args("fsdp_pack_reduce_scatter_noalloc", layout, grads=grads, buckets=bucket_bufs)
+    _check(_lib.fsdp_pack_reduce_scatter_noalloc(layout.handle, g, b, _stream(stream)),
+           "fsdp_pack_reduce_scatter_noalloc")
 
 
 def fsdp_sync_status(layout: Layout, stream=None) -> None:
