@@ -491,6 +491,7 @@ constexpr int kSlotsLarge = FSDP_MAX_PARAMS + 2;
 static_assert(sizeof(LaunchArgs<kSlotsLarge>) <= 32764, "parameter block too large");
 
 std::atomic<int32_t> g_fault{0};
+std::atomic<int32_t> g_upload_fault{0};  // fsdp_debug_set_upload_fault
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 
 template <int NSLOT>
@@ -829,6 +830,8 @@ fsdp_status_t device_setup(fsdp_layout *L) {
   }
   // One allocation: the status word (padded to 32 bytes), then the work table.
   const size_t table_bytes = L->items.size() * sizeof(WorkItem);
+  if (g_upload_fault.load(std::memory_order_relaxed))
+    return fail(FSDP_ENOMEM, "cudaMalloc of the work table: simulated failure (fsdp_debug_set_upload_fault)");
   void *mem = nullptr;
   e = cudaMalloc(&mem, 32 + table_bytes);
   if (e != cudaSuccess)
@@ -1188,6 +1191,10 @@ fsdp_status_t fsdp_pack_reduce_scatter_noalloc(const fsdp_layout_t *L, const voi
   if (P + B <= kSlotsSmall) return noalloc_launch<kSlotsSmall>(table, count, status, grid, ptrs, P + B, s);
   if (P + B <= kSlotsMedium) return noalloc_launch<kSlotsMedium>(table, count, status, grid, ptrs, P + B, s);
   return noalloc_launch<kSlotsLarge>(table, count, status, grid, ptrs, P + B, s);
+}
+
+void fsdp_debug_set_upload_fault(int32_t fail_upload) {
+  g_upload_fault.store(fail_upload ? 1 : 0, std::memory_order_relaxed);
 }
 
 void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns) {

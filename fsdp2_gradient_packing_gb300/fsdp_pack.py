@@ -97,6 +97,7 @@ _SIGNATURES = {
     "fsdp_pack_reduce_scatter_noalloc": (_ST, [_LAYOUT, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "fsdp_sync_status": (_ST, [_LAYOUT, _P]),
     "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
+    "fsdp_debug_set_upload_fault": (None, [ctypes.c_int32]),
     "fsdp_layout_destroy": (None, [_LAYOUT]),
     "fsdp_status_string": (ctypes.c_char_p, [_ST]),
     "fsdp_last_error": (ctypes.c_char_p, []),
@@ -526,6 +527,10 @@ def fsdp_sync_status(layout: Layout, stream=None) -> None:
 
 def fsdp_debug_set_wait_fault(fault: int, wait_limit_ns: int) -> None:
     _lib.fsdp_debug_set_wait_fault(fault, wait_limit_ns)
+
+
+def fsdp_debug_set_upload_fault(fail_upload: bool) -> None:
+    _lib.fsdp_debug_set_upload_fault(1 if fail_upload else 0)
 
 
 def fsdp_layout_destroy(layout: Layout) -> None:

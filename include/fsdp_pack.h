@@ -367,6 +367,16 @@ fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream);
  */
 void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns);
 
+/*
+ * Test hook, process-wide.  While fail_upload is non-zero, planning with a
+ * device table (fsdp_plan_layout, fsdp_plan_layout_ex without
+ * FSDP_PLAN_HOST_ONLY) stops where it would allocate the table and returns
+ * FSDP_ENOMEM, as a failed cudaMalloc does: nothing is allocated, *out stays
+ * NULL.  Layouts planned before are unaffected.  Call with 0 to restore
+ * normal operation.
+ */
+void fsdp_debug_set_upload_fault(int32_t fail_upload);
+
 /* Free the layout and its device work table.  NULL is ignored.  The caller
  * makes sure no launched call still reads the table (synchronise first). */
 void fsdp_layout_destroy(fsdp_layout_t *L);

@@ -659,3 +659,39 @@ def test_bounded_wait_reports_timeout_and_recovers(fp):
         assert out.guards_ok()
     finally:
         run.close()
+
+
+def test_device_table_allocation_failure_reports_enomem(fp):
+    """A failed allocation of the device work table (simulated by the test
+    hook at the point of the cudaMalloc, so nothing is exhausted) gives
+    FSDP_ENOMEM and no layout; a layout planned before keeps working, and
+    planning works again once the hook is off."""
+    work = wl.transformer_500(W=8, layers=1)
+    specs = work.groups[0]
+    run = GroupRun(fp, specs, 8, work, 0)
+    try:
+        grads = [DevBuf(g.nbytes, 0, g) for g in run.grads]
+        out = DevBuf(8 * run.pl.bucket_S[0] * 4)
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        fp.fsdp_debug_set_upload_fault(True)
+        try:
+            for plan in (lambda: fp.fsdp_plan_layout(specs, 8),
+                         lambda: fp.fsdp_plan_layout_ex(specs, 8, fp.row_elems_of(specs))):
+                with pytest.raises(fp.FsdpError) as e:
+                    plan()
+                assert e.value.status == fp.FSDP_ENOMEM
+                assert "simulated" in fp.fsdp_last_error()
+            with fp.fsdp_plan_layout_host(specs, 8):  # host-only planning allocates no device table
+                pass
+            fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [out.ptr])
+            fp.fsdp_sync_status(run.L)
+        finally:
+            fp.fsdp_debug_set_upload_fault(False)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0, "a refused plan kept device memory"
+        assert np.array_equal(out.read(np.uint32), run.pack_expected()[0])
+        with fp.fsdp_plan_layout(specs, 8) as L:
+            assert fp.fsdp_layout_query(L).has_device_table
+    finally:
+        run.close()
