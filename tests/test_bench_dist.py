@@ -61,3 +61,15 @@ def test_reference_arm_prints_one_line(capsys):
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["metric"] == bench.METRIC and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+
+
+def test_reference_arm_runs_on_rank_0_only(capsys, monkeypatch):
+    """Under torchrun with N > 1 the reference arm (the CPU oracle) runs and
+    prints on rank 0 alone; any other rank returns at once, printing nothing."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    bench.main(["--impl", "reference", "--gpus", "2", "--steps", "40", "--warmup", "2"])
+    assert capsys.readouterr().out.strip() == ""
