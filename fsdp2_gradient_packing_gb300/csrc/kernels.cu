@@ -712,12 +712,15 @@ fsdp_status_t check_layout(const fsdp_layout *L) {
   return FSDP_OK;
 }
 
+std::string arg_name(const char *what, int64_t index) {
+  return std::string(what) + (index >= 0 ? "[" + std::to_string(index) + "]" : "");
+}
+
 fsdp_status_t check_ptr(const void *p, int64_t bytes, int64_t align, const char *what, int64_t index) {
   if (bytes == 0) return FSDP_OK;
-  std::string name = std::string(what) + (index >= 0 ? "[" + std::to_string(index) + "]" : "");
-  if (!p) return fail(FSDP_EINVAL, name + " is NULL");
+  if (!p) return fail(FSDP_EINVAL, arg_name(what, index) + " is NULL");
   if (((uintptr_t)p) % (uintptr_t)align)
-    return fail(FSDP_EINVAL, name + " is not " + std::to_string(align) + "-byte aligned");
+    return fail(FSDP_EINVAL, arg_name(what, index) + " is not " + std::to_string(align) + "-byte aligned");
   return FSDP_OK;
 }
 
