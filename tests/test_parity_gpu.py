@@ -40,6 +40,36 @@ def test_random_layouts_misaligned_with_special_values(fp, chunk):
         assert_group_parity(fp, work.groups[0], work.W, work, 0, misalign_seed=seed, specials=0.05)
 
 
+ODD_WORLD_SIZES = (1, 2, 3, 5, 6, 7, 8, 9, 12, 13, 16, 31, 64, 100, 128)
+
+
+@pytest.mark.parametrize("chunk", range(4))
+def test_random_layouts_odd_world_sizes(fp, chunk):
+    """Wider random layouts (up to 12 parameters of up to 40,000 elements, so
+    runs span several work items) at world sizes that divide nothing, both
+    chunking rules, every buffer at a random phase, special values."""
+    for seed in range(20000 + chunk * 100, 20000 + (chunk + 1) * 100):
+        work = wl.random_layout(seed, max_params=12, max_numel=40000, W_choices=ODD_WORLD_SIZES)
+        assert_group_parity(fp, work.groups[0], work.W, work, 0, misalign_seed=seed, specials=0.05)
+    for seed in range(30000 + chunk * 40, 30000 + (chunk + 1) * 40):
+        work = wl.random_layout_2d(seed, max_params=8, max_rows=400, max_row=96, W_choices=ODD_WORLD_SIZES)
+        assert_group_parity(fp, work.groups[0], work.W, work, 0, misalign_seed=seed, specials=0.05, rows=True)
+
+
+@pytest.mark.parametrize("batch", range(8))
+def test_batched_random_layouts_odd_world_sizes(fp, batch):
+    rnd = np.random.default_rng(40000 + batch)
+    runs = []
+    try:
+        for k in range(int(rnd.integers(2, 20))):
+            work = wl.random_layout(50000 + 32 * batch + k, max_params=8, max_numel=30000, W_choices=ODD_WORLD_SIZES)
+            runs.append(GroupRun(fp, work.groups[0], work.W, work, 0, misalign_seed=batch * 32 + k, specials=0.02))
+        assert_batched_parity(fp, runs)
+    finally:
+        for run in runs:
+            run.close()
+
+
 def test_random_long_runs_misaligned(fp):
     # runs long enough to span several work items and pipeline stages
     for seed in range(12):
