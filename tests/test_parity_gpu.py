@@ -527,9 +527,10 @@ def test_torch_tensors_of_the_layout_dtypes_are_accepted_and_checked(fp):
 
 
 def test_flow_around_torch_collectives(fp):
-    """The README's flow on a one-rank NCCL process group (the collectives are
-    then copies): pack, reduce_scatter_tensor, reduce-scatter copy-out;
-    copy-in, all_gather_into_tensor, copy-out; every output against the oracle."""
+    """The calls around torch.distributed's collectives, as a user makes them,
+    on a one-rank NCCL process group (the collectives are then copies): pack,
+    reduce_scatter_tensor, reduce-scatter copy-out; copy-in,
+    all_gather_into_tensor, copy-out; every output against the oracle."""
     import socket
     import torch.distributed as dist
     with socket.socket() as sk:
