@@ -31,9 +31,11 @@ rounded to the bucket dtype) for end-to-end tests without a network.
 
 Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 values the pages print, closed forms, invariants, brute force on tiny inputs
-and an exact-rational rounding reference.  PARITY UNPINNED beyond element
-counts: the split of a multi-parameter unit (this oracle chunks each parameter
-separately; the pages never print such a shard's values).
+and an exact-rational rounding reference.  One reading stands behind them: a
+multi-parameter unit is chunked per parameter (FSDP2's rule), which the brute
+force and the printed per-rank counts pin; the pages print shard values only
+for single-parameter units, where FSDP1's one flat vector split W ways gives
+the same result.
 """
 from __future__ import annotations
 

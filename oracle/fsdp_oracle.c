@@ -32,10 +32,14 @@
  *     (shard dtype, param dtype), each group starting on a 16-byte boundary,
  *     gap and tail bytes zero.
  *
- * Parity pins live in tests/test_oracle_pins.py.  One choice is PARITY
- * UNPINNED beyond element counts: whether a multi-parameter unit is chunked
- * per parameter (this oracle) or as one concatenated flat vector; the pages
- * print values only for single-parameter units.
+ * Parity pins live in tests/test_oracle_pins.py.  A multi-parameter unit is
+ * chunked per parameter (FSDP2's rule: every parameter padded and split into
+ * W chunks, rank r's row the concatenation of the chunks r), which is a
+ * reading: the pages print shard values only for single-parameter units,
+ * where it agrees with FSDP1's one flat vector split W ways.  The
+ * per-parameter rule is pinned by brute force (pad, reshape, concatenate) on
+ * every one- and two-parameter layout up to 13 elements and W = 5, on sampled
+ * three-parameter layouts, and by the per-rank counts the pages print.
  *
  * Dtype codes used by this file only: 0 = FP32, 1 = BF16.
  */
