@@ -4,7 +4,6 @@ does, and rejects bad arguments with the documented status codes."""
 import ctypes
 import glob
 import os
-import random
 import re
 
 import pytest
