@@ -79,6 +79,21 @@ constexpr uint32_t kStatusBadItem = 8u;
 // stage's consumers time out (no fault, no hang: every wait is bounded).
 constexpr int32_t kFaultSkipFirstStage = 1;
 
+// How a launch hands out its n work items to its G CTAs.  CTA b first takes
+// items b + m*G for m < fixed_rounds, in that fixed order.  The rest, items
+// [fixed_rounds*G, n), go to whichever CTA asks first, through a work-sharing
+// word in device memory (one per layout and operation); with word == nullptr
+// they follow the fixed order too.  See sched_join for the word's protocol.
+struct Sched {
+  unsigned long long *word;
+  int64_t fixed_rounds;
+  uint32_t tag;   // this launch's owner tag: nonzero, 24 bits
+  int32_t flags;  // kSchedMixed
+};
+// Test hook: CTAs with an odd index act as if another launch held the word,
+// so one launch mixes CTAs that share the word with CTAs in the fixed order.
+constexpr int32_t kSchedMixed = 1;
+
 // Per-call pointers travel by value in the parameter block: `slot` is read
 // with a run-time index, which __grid_constant__ allows without a local copy.
 // fetch(i) returns work item i and the slot base its slot numbers are
@@ -91,6 +106,7 @@ struct LaunchArgs {
   uint64_t wait_limit_ns;
   int32_t fault;
   int32_t reserved;
+  Sched sched;
   const void *slot[NSLOT];
 
   __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base) const {
@@ -109,6 +125,7 @@ struct BatchArgs {
   uint64_t wait_limit_ns;
   int32_t fault;
   int32_t n_groups;
+  Sched sched;
   const WorkItem *items[kMaxBatch];
   int64_t start[kMaxBatch + 1];
   int32_t slot_base[kMaxBatch];
@@ -294,6 +311,57 @@ struct StageHeader {
 };
 static_assert(sizeof(StageHeader) <= kHeaderBytes, "stage header too large");
 constexpr int32_t kSkipItem = -1;
+constexpr int32_t kDoneItem = -2;  // no item follows: the consumers leave
+
+// The work-sharing word: bits 0..23 count the items handed out since the
+// word was taken, bits 24..39 count the CTAs taking items from it ("users"),
+// bits 40..63 hold the tag of the launch that took it (0: never taken).
+//   * A CTA joins after its fixed-order items.  If the word carries its own
+//     launch's tag, it adds itself as a user, and stays one if the tag is
+//     still its own in the value the add returns (else it undoes the add).
+//     If the word has no users, the CTA takes it for its launch with one
+//     compare-and-swap: its tag, one user, count 0.  If another launch's
+//     CTAs are using it, the CTA does not join.
+//   * A user takes item fixed_rounds*G + (count before its add) by adding 1,
+//     and leaves (removes itself as a user) on the first index past the end.
+//   * A CTA that does not join takes the rest of its fixed order,
+//     b + m*G for m >= fixed_rounds.
+// Only the launch holding the word adds to its count, and the word changes
+// hands only while it has no users, which happens after every user saw the
+// end of the count: so when any CTA of a launch joins, that launch's users
+// take every shared item between them; when none joins, the fixed order
+// covers them.  A CTA that does not join may repeat items a user took; the
+// second copy writes the same bytes, as every item's output depends on the
+// inputs only.  Launches of one layout that overlap on the GPU (different
+// streams) therefore give the same results as launches in turn.  The host
+// keeps the shared part below 2^22 items so the count never reaches bit 24.
+constexpr unsigned long long kSchedUser = 1ull << 24;
+constexpr unsigned long long kSchedCountMask = kSchedUser - 1;
+__device__ __forceinline__ uint32_t sched_tag_of(unsigned long long v) { return (uint32_t)(v >> 40); }
+__device__ __forceinline__ uint32_t sched_users_of(unsigned long long v) { return (uint32_t)(v >> 24) & 0xFFFFu; }
+
+__device__ __forceinline__ unsigned long long load_relaxed(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ bool sched_join(unsigned long long *word, uint32_t tag) {
+  unsigned long long v = load_relaxed(word);
+  for (int attempt = 0; attempt < 4; ++attempt) {
+    if (sched_tag_of(v) == tag) {
+      const unsigned long long r = atomicAdd(word, kSchedUser);
+      if (sched_tag_of(r) == tag) return true;
+      atomicAdd(word, 0ull - kSchedUser);  // taken by another launch meanwhile
+      return false;
+    }
+    if (sched_users_of(v) != 0) return false;
+    const unsigned long long c = atomicCAS(word, v, ((unsigned long long)tag << 40) | kSchedUser);
+    if (c == v) return true;
+    v = c;
+  }
+  return false;
+}
 
 // Consumer side of one item.  `stage` holds the item's staged source.
 // `ct` is the consumer thread index in [0, kConsumers).  Each thread handles
@@ -408,23 +476,62 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
   const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
   if (warp == 0) {
     if (lane != 0) return;
-    // Producer.  The next item's descriptor is fetched one item ahead; the
-    // first one before waiting for the previous kernel on the stream.
+    // Producer.  Item indices are claimed two items ahead of use and their
+    // descriptors fetched one ahead, so neither the work-sharing word's
+    // round trip nor the descriptor load sits on a stage hand-off.
+    const int64_t G = gridDim.x, n = a.n_items;
+    const Sched sc = a.sched;
+    const int64_t shared0 = sc.word ? sc.fixed_rounds * G : 0;  // first shared item
+    // part 0: fixed-order items; 1: user of the word; 2: fixed order over
+    // [shared0, n); 3: nothing left.
+    int part = sc.word ? 0 : 2;
+    int64_t m = 0;
+    auto claim = [&]() -> int64_t {
+      if (part == 0) {
+        if (m < sc.fixed_rounds) return (int64_t)blockIdx.x + (m++) * G;
+        m = 0;
+        const bool mixed_out = (sc.flags & kSchedMixed) && (blockIdx.x & 1u);
+        part = !mixed_out && sched_join(sc.word, sc.tag) ? 1 : 2;
+      }
+      if (part == 1) {
+        const int64_t i = shared0 + (int64_t)(atomicAdd(sc.word, 1ull) & kSchedCountMask);
+        if (i < n) return i;
+        atomicAdd(sc.word, 0ull - kSchedUser);  // leave
+        part = 3;
+        return n;
+      }
+      if (part == 2) return shared0 + (int64_t)blockIdx.x + (m++) * G;
+      return n;
+    };
     int64_t k = 0;
-    bool skipped_first = false;
-    int64_t i = blockIdx.x;
-    WorkItem next{};
-    int32_t next_base = 0;
-    if (i < a.n_items) next = a.fetch(i, &next_base);
+    bool skipped_first = false, stopped = false;
+    WorkItem cur{};
+    int32_t cur_base = 0;
+    // The first descriptor is fetched before waiting for the previous kernel
+    // on the stream, unless getting its index means joining the word: a
+    // launch of the same operation may still hold it until that wait.
+    const bool early = part == 2 || sc.fixed_rounds > 0;
+    int64_t c0 = n;
+    if (early) {
+      c0 = claim();
+      if (c0 < n) cur = a.fetch(c0, &cur_base);
+    }
     wait_for_previous_grid();
-    for (; i < a.n_items; i += gridDim.x, ++k) {
-      const WorkItem w = next;
-      const int32_t base = next_base;
-      if (i + gridDim.x < a.n_items) next = a.fetch(i + gridDim.x, &next_base);
+    if (!early) {
+      c0 = claim();
+      if (c0 < n) cur = a.fetch(c0, &cur_base);
+    }
+    int64_t c1 = claim(), c2 = n;
+    for (; c0 < n; ++k, c0 = c1, c1 = c2) {
+      const WorkItem w = cur;
+      const int32_t base = cur_base;
+      c2 = claim();
+      if (c1 < n) cur = a.fetch(c1, &cur_base);
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
         atomicOr(a.status, kStatusProducerWait);
+        stopped = true;
         break;
       }
       if (k == 0 && blockIdx.x == 0 && (a.fault & kFaultSkipFirstStage)) {
@@ -449,27 +556,41 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       mbar_arrive_expect_tx(&full[s], bytes);
       if (bytes) bulk_copy_g2s(smem + s * kStageStride, src - st.lead, bytes, &full[s]);
     }
+    if (part == 1) atomicAdd(sc.word, 0ull - kSchedUser);  // stopped early: leave
     // Leave no bulk copy in flight when this thread exits: wait for the last
-    // armed phase of every stage (consumers may have left early).
+    // armed phase of every stage (consumers may have left early).  This comes
+    // before the end marker below, which completes one more phase of a stage.
     for (int64_t kk = k > kStages ? k - kStages : 0; kk < k; ++kk) {
       if (kk == 0 && skipped_first) continue;
       if (!mbar_wait(&full[kk % kStages], (uint32_t)(kk / kStages) & 1u, a.wait_limit_ns))
         atomicOr(a.status, kStatusDrainWait);
     }
+    // Tell the consumers that no item follows: a header of kind kDoneItem in
+    // the next stage, its phase completed by a plain arrive.
+    if (!stopped) {
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      if (round == 0 || mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
+        reinterpret_cast<StageHeader *>(smem + s * kStageStride + kStageDataBytes)->kind = kDoneItem;
+        mbar_arrive(&full[s]);
+      } else {
+        atomicOr(a.status, kStatusProducerWait);
+      }
+    }
     return;
   }
 
-  // Consumers.
+  // Consumers: the items come in stage order until an end marker.
   wait_for_previous_grid();
   const int ct = (int)threadIdx.x - 32;
-  int64_t k = 0;
-  for (int64_t i = blockIdx.x; i < a.n_items; i += gridDim.x, ++k) {
+  for (int64_t k = 0;; ++k) {
     const int s = (int)(k % kStages);
     if (!mbar_wait(&full[s], (uint32_t)(k / kStages) & 1u, a.wait_limit_ns)) {
       if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
       return;
     }
     const StageHeader hd = *reinterpret_cast<const StageHeader *>(smem + s * kStageStride + kStageDataBytes);
+    if (hd.kind == kDoneItem) return;
     const uint8_t *stage = smem + s * kStageStride;
     switch (hd.kind) {
       case KIND_F32_F32: consume_item<KIND_F32_F32>(hd.src, hd.dst, hd.n_copy, hd.n_total, stage, ct); break;
@@ -493,6 +614,34 @@ static_assert(sizeof(LaunchArgs<kSlotsLarge>) <= 32764, "parameter block too lar
 std::atomic<int32_t> g_fault{0};
 std::atomic<int32_t> g_upload_fault{0};  // fsdp_debug_set_upload_fault
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int32_t> g_sched_mode{FSDP_SCHEDULE_DEFAULT};  // fsdp_debug_set_schedule
+
+// A launch shares its last quarter of items when it has at least
+// kSharedMinRounds items per CTA; smaller launches keep the fixed order,
+// where the word's round trips would cost more than the balance gains.
+constexpr int64_t kSharedMinRounds = 8;
+constexpr int64_t kSharedMaxItems = int64_t(1) << 22;  // keeps the count below bit 24
+
+// The schedule of one launch of n items on `grid` CTAs.  `word` is the
+// operation's work-sharing word (nullptr: fixed order) and `epoch` the host
+// counter its tags come from: tags run 1 .. 2^24 - 1 and wrap, so a tag is
+// reused only after 16.7M launches on one word.
+Sched make_sched(unsigned long long *word, std::atomic<uint32_t> *epoch, int64_t n, int64_t grid) {
+  Sched sc{nullptr, 0, 0, 0};
+  const int32_t mode = g_sched_mode.load(std::memory_order_relaxed);
+  if (!word || !epoch || grid <= 0 || mode == FSDP_SCHEDULE_FIXED) return sc;
+  int64_t rounds = 0;
+  if (mode == FSDP_SCHEDULE_DEFAULT) {
+    if (n < kSharedMinRounds * grid) return sc;
+    rounds = (n / grid) * 3 / 4;
+  }
+  if (n - rounds * grid > kSharedMaxItems) rounds = (n - kSharedMaxItems + grid - 1) / grid;
+  sc.word = word;
+  sc.fixed_rounds = rounds;
+  sc.tag = epoch->fetch_add(1, std::memory_order_relaxed) % 0xFFFFFFu + 1u;
+  sc.flags = mode == FSDP_SCHEDULE_MIXED ? kSchedMixed : 0;
+  return sc;
+}
 
 template <int NSLOT>
 fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptrs, int n_ptrs,
@@ -504,6 +653,7 @@ fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptr
   a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   a.fault = g_fault.load(std::memory_order_relaxed);
   a.reserved = 0;
+  a.sched = make_sched(L->d_sched + op, &L->sched_epoch[op], a.n_items, L->op[op].grid);
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
   // Programmatic stream serialization: this launch may be scheduled while the
@@ -569,6 +719,7 @@ fsdp_status_t batch_launch_variant(const fsdp_layout *const *Ls, int n, Op op, c
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
   const int64_t grid = total < Ls[0]->resident ? total : Ls[0]->resident;
+  a.sched = make_sched(Ls[0]->d_sched + op, &Ls[0]->sched_epoch[op], total, grid);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -790,6 +941,7 @@ fsdp_status_t noalloc_launch(const WorkItem *items, int64_t n_items, uint32_t *s
   a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   a.fault = 0;
   a.reserved = 0;
+  a.sched = Sched{nullptr, 0, 0, 0};  // fixed order: the array holds no work-sharing word
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
   cudaLaunchAttribute attr[1];
@@ -831,22 +983,27 @@ fsdp_status_t device_setup(fsdp_layout *L) {
     int64_t g = L->op[op].count < resident ? L->op[op].count : resident;
     L->op[op].grid = (int32_t)(g > 0 ? g : 0);
   }
-  // One allocation: the status word (padded to 32 bytes), then the work table.
+  // One allocation: a 64-byte header -- the status word at byte 0, one
+  // work-sharing word per operation from byte 32 -- then the work table.
+  constexpr size_t kHeader = 64;
+  static_assert(32 + OP_COUNT * sizeof(unsigned long long) <= kHeader, "device header too small");
   const size_t table_bytes = L->items.size() * sizeof(WorkItem);
   if (g_upload_fault.load(std::memory_order_relaxed))
     return fail(FSDP_ENOMEM, "cudaMalloc of the work table: simulated failure (fsdp_debug_set_upload_fault)");
   void *mem = nullptr;
-  e = cudaMalloc(&mem, 32 + table_bytes);
+  e = cudaMalloc(&mem, kHeader + table_bytes);
   if (e != cudaSuccess)
     return fail(FSDP_ENOMEM, std::string("cudaMalloc of the work table: ") + cudaGetErrorString(e));
   L->d_status = reinterpret_cast<uint32_t *>(mem);
-  L->d_items = reinterpret_cast<WorkItem *>(reinterpret_cast<char *>(mem) + 32);
-  e = cudaMemset(mem, 0, 32);
+  L->d_sched = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(mem) + 32);
+  L->d_items = reinterpret_cast<WorkItem *>(reinterpret_cast<char *>(mem) + kHeader);
+  e = cudaMemset(mem, 0, kHeader);
   if (e == cudaSuccess && table_bytes)
     e = cudaMemcpy(L->d_items, L->items.data(), table_bytes, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(mem);
     L->d_status = nullptr;
+    L->d_sched = nullptr;
     L->d_items = nullptr;
     return fail(FSDP_ECUDA, std::string("work table upload: ") + cudaGetErrorString(e));
   }
@@ -862,6 +1019,7 @@ void device_release(fsdp_layout *L) {
   cudaFree(L->d_status);
   if (switched) cudaSetDevice(cur);
   L->d_status = nullptr;
+  L->d_sched = nullptr;
   L->d_items = nullptr;
 }
 
@@ -1204,6 +1362,14 @@ void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns) {
   g_fault.store(fault, std::memory_order_relaxed);
   g_wait_limit_ns.store(wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kDefaultWaitLimitNs,
                         std::memory_order_relaxed);
+}
+
+fsdp_status_t fsdp_debug_set_schedule(int32_t mode) {
+  if (mode < FSDP_SCHEDULE_DEFAULT || mode > FSDP_SCHEDULE_MIXED)
+    return fail(FSDP_EINVAL, "unknown schedule mode " + std::to_string(mode));
+  g_sched_mode.store(mode, std::memory_order_relaxed);
+  clear_error();
+  return FSDP_OK;
 }
 
 }  // extern "C"

@@ -2,6 +2,7 @@
 // device side (kernels.cu).  Not part of the C ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -95,6 +96,9 @@ struct fsdp_layout {
   int32_t sms = 0;                     // SMs of the device
   fsdp::WorkItem *d_items = nullptr;   // device copy of `items`
   uint32_t *d_status = nullptr;        // device status word (bounded-wait failures)
+  unsigned long long *d_sched = nullptr;  // one work-sharing word per operation (device)
+  // Host counters of the owner tags that launches put in those words.
+  mutable std::atomic<uint32_t> sched_epoch[fsdp::OP_COUNT]{};
 };
 
 namespace fsdp {

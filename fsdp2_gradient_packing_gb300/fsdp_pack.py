@@ -32,6 +32,7 @@ DTYPE_BYTES = {FSDP_DTYPE_F32: 4, FSDP_DTYPE_BF16: 2}
 FSDP_OK, FSDP_EINVAL, FSDP_ENOMEM, FSDP_ECUDA, FSDP_EUNSUPPORTED, FSDP_ETIMEOUT = range(6)
 FSDP_MAX_PARAMS = 4000
 FSDP_PLAN_HOST_ONLY = 1
+FSDP_SCHEDULE_DEFAULT, FSDP_SCHEDULE_FIXED, FSDP_SCHEDULE_SHARED, FSDP_SCHEDULE_MIXED = range(4)
 
 
 class fsdp_param_desc_t(ctypes.Structure):
@@ -98,6 +99,7 @@ _SIGNATURES = {
     "fsdp_sync_status": (_ST, [_LAYOUT, _P]),
     "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
     "fsdp_debug_set_upload_fault": (None, [ctypes.c_int32]),
+    "fsdp_debug_set_schedule": (_ST, [ctypes.c_int32]),
     "fsdp_layout_destroy": (None, [_LAYOUT]),
     "fsdp_status_string": (ctypes.c_char_p, [_ST]),
     "fsdp_last_error": (ctypes.c_char_p, []),
@@ -531,6 +533,10 @@ def fsdp_debug_set_wait_fault(fault: int, wait_limit_ns: int) -> None:
 
 def fsdp_debug_set_upload_fault(fail_upload: bool) -> None:
     _lib.fsdp_debug_set_upload_fault(1 if fail_upload else 0)
+
+
+def fsdp_debug_set_schedule(mode: int) -> None:
+    _check(_lib.fsdp_debug_set_schedule(mode), "fsdp_debug_set_schedule")
 
 
 def fsdp_layout_destroy(layout: Layout) -> None:

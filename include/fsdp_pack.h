@@ -42,8 +42,11 @@
  *   - Arguments are checked on the host before anything is launched.  On any
  *     error nothing is launched, the status says why, and fsdp_last_error()
  *     returns a one-line description for the calling thread.
- *   - A layout may be used from several host threads at once (it is only
- *     read after planning).
+ *   - A layout may be used from several host threads at once (its tables are
+ *     only read after planning), and its calls may overlap on the GPU on
+ *     different streams: the one device word per operation that lets a
+ *     launch balance its last items across the GPU's blocks is never shared
+ *     between two launches at once (see fsdp_debug_set_schedule).
  */
 #ifndef FSDP_PACK_H
 #define FSDP_PACK_H
@@ -366,6 +369,35 @@ fsdp_status_t fsdp_sync_status(const fsdp_layout_t *L, fsdp_stream_t stream);
  * restore normal operation.
  */
 void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns);
+
+/*
+ * Test hook, process-wide: how the next launches hand out their work items
+ * to the kernel's blocks.  Results are the same in every mode.
+ *   FSDP_SCHEDULE_DEFAULT  a launch with at least 8 items per block gives
+ *                          each block 3/4 of its share in a fixed order and
+ *                          hands out the rest to whichever block asks first,
+ *                          through a small device word of the layout (one per
+ *                          operation).  A launch that finds the word in use
+ *                          by another launch of the same layout and operation
+ *                          (calls overlapping on different streams) keeps
+ *                          the fixed order for the rest.  Smaller launches
+ *                          and fsdp_pack_reduce_scatter_noalloc keep the
+ *                          fixed order throughout.
+ *   FSDP_SCHEDULE_FIXED    every launch keeps the fixed order: block b takes
+ *                          items b, b + G, b + 2G, ... of its G blocks.
+ *   FSDP_SCHEDULE_SHARED   every launch with a device table hands out all its
+ *                          items through the word, at any size.
+ *   FSDP_SCHEDULE_MIXED    as FSDP_SCHEDULE_SHARED, but blocks with an odd
+ *                          index act as if another launch held the word.
+ * Returns FSDP_EINVAL (and changes nothing) for any other mode.
+ */
+typedef enum {
+  FSDP_SCHEDULE_DEFAULT = 0,
+  FSDP_SCHEDULE_FIXED = 1,
+  FSDP_SCHEDULE_SHARED = 2,
+  FSDP_SCHEDULE_MIXED = 3
+} fsdp_schedule_t;
+fsdp_status_t fsdp_debug_set_schedule(int32_t mode);
 
 /*
  * Test hook, process-wide.  While fail_upload is non-zero, planning with a

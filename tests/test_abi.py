@@ -251,3 +251,13 @@ def test_plan_without_gpu_reports_cuda_error(fp):
     with pytest.raises(fp.FsdpError) as e:
         fp.fsdp_plan_layout(wl.tiny_two_blocks().groups[0], 4)
     assert e.value.status == fp.FSDP_ECUDA
+
+
+def test_schedule_hook_accepts_its_modes_and_refuses_others(fp):
+    for mode in (fp.FSDP_SCHEDULE_FIXED, fp.FSDP_SCHEDULE_SHARED, fp.FSDP_SCHEDULE_MIXED,
+                 fp.FSDP_SCHEDULE_DEFAULT):
+        fp.fsdp_debug_set_schedule(mode)
+    for bad in (-1, 4, 1 << 20):
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_debug_set_schedule(bad)
+        assert e.value.status == fp.FSDP_EINVAL and "unknown schedule mode" in str(e.value)
