@@ -97,7 +97,7 @@ constexpr int32_t kSchedMixed = 1;
 // Per-call pointers travel by value in the parameter block: `slot` is read
 // with a run-time index, which __grid_constant__ allows without a local copy.
 // fetch(i) returns work item i and the slot base its slot numbers are
-// relative to.
+// relative to; `cursor` carries the layout of the CTA's previous item.
 template <int NSLOT>
 struct LaunchArgs {
   const WorkItem *items;
@@ -109,7 +109,7 @@ struct LaunchArgs {
   Sched sched;
   const void *slot[NSLOT];
 
-  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base) const {
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *) const {
     *base = 0;
     return items[i];
   }
@@ -131,15 +131,18 @@ struct BatchArgs {
   int32_t slot_base[kMaxBatch];
   const void *slot[NSLOT];
 
-  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base) const {
-    int lo = 0, hi = n_groups - 1;  // the last group that starts at or before i
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (start[mid] <= i) lo = mid;
-      else hi = mid - 1;
-    }
-    *base = slot_base[lo];
-    return items[lo][i - start[lo]];
+  // The last group that starts at or before i, found by walking forward
+  // from the CTA's previous one: a CTA's item indices grow (except after the
+  // rare retake of the work-sharing word, which restarts the walk), so the
+  // walk costs about one step per layout instead of a chain of dependent
+  // parameter loads per item.
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *cursor) const {
+    int g = *cursor;
+    if (start[g] > i) g = 0;
+    while (g + 1 < n_groups && start[g + 1] <= i) ++g;
+    *cursor = g;
+    *base = slot_base[g];
+    return items[g][i - start[g]];
   }
 };
 
@@ -478,7 +481,9 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     if (lane != 0) return;
     // Producer.  Item indices are claimed two items ahead of use and their
     // descriptors fetched one ahead, so neither the work-sharing word's
-    // round trip nor the descriptor load sits on a stage hand-off.
+    // round trip nor the descriptor load sits on a stage hand-off: issue()
+    // starts a claim without looking at what a shared claim's atomic add
+    // returns, and resolve() turns it into an index one item later.
     const int64_t G = gridDim.x, n = a.n_items;
     const Sched sc = a.sched;
     const int64_t shared0 = sc.word ? sc.fixed_rounds * G : 0;  // first shared item
@@ -486,47 +491,63 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     // [shared0, n); 3: nothing left.
     int part = sc.word ? 0 : 2;
     int64_t m = 0;
-    auto claim = [&]() -> int64_t {
+    struct Claim {
+      unsigned long long v;  // an item index, or the word's value before a shared claim's add
+      bool shared;
+    };
+    auto issue = [&]() -> Claim {
       if (part == 0) {
-        if (m < sc.fixed_rounds) return (int64_t)blockIdx.x + (m++) * G;
+        if (m < sc.fixed_rounds) return Claim{(unsigned long long)(blockIdx.x + (m++) * G), false};
         m = 0;
         const bool mixed_out = (sc.flags & kSchedMixed) && (blockIdx.x & 1u);
         part = !mixed_out && sched_join(sc.word, sc.tag) ? 1 : 2;
       }
+      if (part == 1) return Claim{atomicAdd(sc.word, 1ull), true};
+      if (part == 2) return Claim{(unsigned long long)(shared0 + blockIdx.x + (m++) * G), false};
+      return Claim{(unsigned long long)n, false};
+    };
+    // Claims resolve in the order they were issued.  Shared counts only grow
+    // while this CTA is a user, so after the first shared claim past the end
+    // every later one is past it too; the CTA leaves on the first.  Its adds
+    // issued before the leave come first in the word's order (one thread,
+    // one address), so the leave never lands ahead of them.
+    auto resolve = [&](Claim q) -> int64_t {
+      if (!q.shared) return (int64_t)q.v;
+      const int64_t i = shared0 + (int64_t)(q.v & kSchedCountMask);
+      if (i < n) return i;
       if (part == 1) {
-        const int64_t i = shared0 + (int64_t)(atomicAdd(sc.word, 1ull) & kSchedCountMask);
-        if (i < n) return i;
         atomicAdd(sc.word, 0ull - kSchedUser);  // leave
         part = 3;
-        return n;
       }
-      if (part == 2) return shared0 + (int64_t)blockIdx.x + (m++) * G;
       return n;
     };
     int64_t k = 0;
     bool skipped_first = false, stopped = false;
     WorkItem cur{};
     int32_t cur_base = 0;
+    int cursor = 0;  // layout of the last fetched item (batched launches)
     // The first descriptor is fetched before waiting for the previous kernel
     // on the stream, unless getting its index means joining the word: a
     // launch of the same operation may still hold it until that wait.
     const bool early = part == 2 || sc.fixed_rounds > 0;
     int64_t c0 = n;
     if (early) {
-      c0 = claim();
-      if (c0 < n) cur = a.fetch(c0, &cur_base);
+      c0 = resolve(issue());
+      if (c0 < n) cur = a.fetch(c0, &cur_base, &cursor);
     }
     wait_for_previous_grid();
     if (!early) {
-      c0 = claim();
-      if (c0 < n) cur = a.fetch(c0, &cur_base);
+      c0 = resolve(issue());
+      if (c0 < n) cur = a.fetch(c0, &cur_base, &cursor);
     }
-    int64_t c1 = claim(), c2 = n;
-    for (; c0 < n; ++k, c0 = c1, c1 = c2) {
+    Claim q1 = issue(), q2{};
+    int64_t c1 = n;
+    for (; c0 < n; ++k, c0 = c1, q1 = q2) {
       const WorkItem w = cur;
       const int32_t base = cur_base;
-      c2 = claim();
-      if (c1 < n) cur = a.fetch(c1, &cur_base);
+      q2 = issue();
+      c1 = resolve(q1);
+      if (c1 < n) cur = a.fetch(c1, &cur_base, &cursor);
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
@@ -617,8 +638,13 @@ std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int32_t> g_sched_mode{FSDP_SCHEDULE_DEFAULT};  // fsdp_debug_set_schedule
 
 // A launch shares its last quarter of items when it has at least
-// kSharedMinRounds items per CTA; smaller launches keep the fixed order,
-// where the word's round trips would cost more than the balance gains.
+// kSharedMinRounds items per CTA -- a batched launch when its layouts have
+// that many on average; other launches keep the fixed order.  Measured on
+// one GB300: sharing made large single groups 5-8 % faster (blocks on a few
+// slow SMs no longer set the end) and a batch of eight large groups 9 %
+// faster, but a batch of 24 small groups (864 items each) 3 % slower: its
+// fixed order was already balanced, and each shared item costs an atomic
+// round trip on one word.
 constexpr int64_t kSharedMinRounds = 8;
 constexpr int64_t kSharedMaxItems = int64_t(1) << 22;  // keeps the count below bit 24
 
@@ -626,13 +652,14 @@ constexpr int64_t kSharedMaxItems = int64_t(1) << 22;  // keeps the count below 
 // operation's work-sharing word (nullptr: fixed order) and `epoch` the host
 // counter its tags come from: tags run 1 .. 2^24 - 1 and wrap, so a tag is
 // reused only after 16.7M launches on one word.
-Sched make_sched(unsigned long long *word, std::atomic<uint32_t> *epoch, int64_t n, int64_t grid) {
+Sched make_sched(unsigned long long *word, std::atomic<uint32_t> *epoch, int64_t n, int64_t grid,
+                 int64_t n_layouts = 1) {
   Sched sc{nullptr, 0, 0, 0};
   const int32_t mode = g_sched_mode.load(std::memory_order_relaxed);
   if (!word || !epoch || grid <= 0 || mode == FSDP_SCHEDULE_FIXED) return sc;
   int64_t rounds = 0;
   if (mode == FSDP_SCHEDULE_DEFAULT) {
-    if (n < kSharedMinRounds * grid) return sc;
+    if (n < kSharedMinRounds * grid * n_layouts) return sc;
     rounds = (n / grid) * 3 / 4;
   }
   if (n - rounds * grid > kSharedMaxItems) rounds = (n - kSharedMaxItems + grid - 1) / grid;
@@ -719,7 +746,7 @@ fsdp_status_t batch_launch_variant(const fsdp_layout *const *Ls, int n, Op op, c
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
   const int64_t grid = total < Ls[0]->resident ? total : Ls[0]->resident;
-  a.sched = make_sched(Ls[0]->d_sched + op, &Ls[0]->sched_epoch[op], total, grid);
+  a.sched = make_sched(Ls[0]->d_sched + op, &Ls[0]->sched_epoch[op], total, grid, groups);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

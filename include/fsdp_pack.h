@@ -304,7 +304,9 @@ fsdp_status_t fsdp_emulated_reduce_scatter(const fsdp_layout_t *L, const void *c
  *   likewise; ag_inputs and ag_outputs hold one all-gather buffer per layout.  At most 3,840
  *   pointers per batch (FSDP_EUNSUPPORTED above).
  * Outputs of different layouts must not overlap.  A bounded-wait failure is
- * recorded in the first layout's status word (fsdp_sync_status(layouts[0])).
+ * recorded in the first layout's status word (fsdp_sync_status(layouts[0])),
+ * and a batched launch that shares its last items (fsdp_debug_set_schedule)
+ * does so through the first layout's work-sharing word for the operation.
  */
 fsdp_status_t fsdp_pack_reduce_scatter_batched(const fsdp_layout_t *const *layouts, int32_t n_layouts,
                                                const void *const *grads, void *const *bucket_bufs,
@@ -373,7 +375,8 @@ void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns);
 /*
  * Test hook, process-wide: how the next launches hand out their work items
  * to the kernel's blocks.  Results are the same in every mode.
- *   FSDP_SCHEDULE_DEFAULT  a launch with at least 8 items per block gives
+ *   FSDP_SCHEDULE_DEFAULT  a launch with at least 8 items per block (a
+ *                          batched launch: per block and layout) gives
  *                          each block 3/4 of its share in a fixed order and
  *                          hands out the rest to whichever block asks first,
  *                          through a small device word of the layout (one per
