@@ -349,7 +349,7 @@ __device__ __forceinline__ unsigned long long load_relaxed(const unsigned long l
   return v;
 }
 
-__device__ bool sched_join(unsigned long long *word, uint32_t tag) {
+__device__ __noinline__ bool sched_join(unsigned long long *word, uint32_t tag) {
   unsigned long long v = load_relaxed(word);
   for (int attempt = 0; attempt < 4; ++attempt) {
     if (sched_tag_of(v) == tag) {
@@ -523,41 +523,20 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     };
     int64_t k = 0;
     bool skipped_first = false, stopped = false;
-    WorkItem cur{};
-    int32_t cur_base = 0;
     int cursor = 0;  // layout of the last fetched item (batched launches)
-    // The first descriptor is fetched before waiting for the previous kernel
-    // on the stream, unless getting its index means joining the word: a
-    // launch of the same operation may still hold it until that wait.
-    const bool early = part == 2 || sc.fixed_rounds > 0;
-    int64_t c0 = n;
-    if (early) {
-      c0 = resolve(issue());
-      if (c0 < n) cur = a.fetch(c0, &cur_base, &cursor);
-    }
-    wait_for_previous_grid();
-    if (!early) {
-      c0 = resolve(issue());
-      if (c0 < n) cur = a.fetch(c0, &cur_base, &cursor);
-    }
-    Claim q1 = issue(), q2{};
-    int64_t c1 = n;
-    for (; c0 < n; ++k, c0 = c1, q1 = q2) {
-      const WorkItem w = cur;
-      const int32_t base = cur_base;
-      q2 = issue();
-      c1 = resolve(q1);
-      if (c1 < n) cur = a.fetch(c1, &cur_base, &cursor);
+    // Stage item w (slot base `base`) in the ring; false if the stage never
+    // came free (the wait gave up).
+    auto stage_item = [&](const WorkItem &w, int32_t base) -> bool {
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
         atomicOr(a.status, kStatusProducerWait);
-        stopped = true;
-        break;
+        return false;
       }
       if (k == 0 && blockIdx.x == 0 && (a.fault & kFaultSkipFirstStage)) {
         skipped_first = true;
-        continue;
+        ++k;
+        return true;
       }
       const int ss = (w.kind & 1) ? 2 : 4, ds = (w.kind & 2) ? 2 : 4;
       const char *src = reinterpret_cast<const char *>(a.slot[base + w.src_slot]) + w.src_off * (int64_t)ss;
@@ -576,6 +555,56 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       }
       mbar_arrive_expect_tx(&full[s], bytes);
       if (bytes) bulk_copy_g2s(smem + s * kStageStride, src - st.lead, bytes, &full[s]);
+      ++k;
+      return true;
+    };
+    // A CTA's first item is blockIdx.x in every schedule (a launch that
+    // shares items keeps at least one fixed round), so its descriptor is
+    // fetched before waiting for the previous kernel on the stream.
+    int32_t cur_base = 0;
+    WorkItem cur = a.fetch(blockIdx.x, &cur_base, &cursor);  // the grid is at most n
+    wait_for_previous_grid();
+    if (!sc.word) {
+      // Fixed order: items blockIdx.x + m * G, each descriptor fetched one
+      // item ahead.
+      for (int64_t i = blockIdx.x; i < n; i += G) {
+        const WorkItem w = cur;
+        const int32_t base = cur_base;
+        if (i + G < n) cur = a.fetch(i + G, &cur_base, &cursor);
+        if (!stage_item(w, base)) {
+          stopped = true;
+          break;
+        }
+      }
+    } else {
+      // Shared: each round issues the claim two items ahead and resolves the
+      // one issued the round before (a first round only primes that queue),
+      // so neither the word's round trip nor the descriptor load sits on a
+      // stage hand-off.  Joining the word comes after the wait above, when
+      // an earlier launch of the same operation on the stream has let go of
+      // it.
+      m = 1;
+      int64_t c0 = blockIdx.x;
+      Claim q1{};
+      bool primed = false;
+      while (c0 < n) {
+        const Claim qn = issue();
+        if (!primed) {
+          q1 = qn;
+          primed = true;
+          continue;
+        }
+        const WorkItem w = cur;
+        const int32_t base = cur_base;
+        const int64_t c1 = resolve(q1);
+        if (c1 < n) cur = a.fetch(c1, &cur_base, &cursor);
+        q1 = qn;
+        c0 = c1;
+        if (!stage_item(w, base)) {
+          stopped = true;
+          break;
+        }
+      }
     }
     if (part == 1) atomicAdd(sc.word, 0ull - kSchedUser);  // stopped early: leave
     // Leave no bulk copy in flight when this thread exits: wait for the last
@@ -586,9 +615,10 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       if (!mbar_wait(&full[kk % kStages], (uint32_t)(kk / kStages) & 1u, a.wait_limit_ns))
         atomicOr(a.status, kStatusDrainWait);
     }
-    // Tell the consumers that no item follows: a header of kind kDoneItem in
-    // the next stage, its phase completed by a plain arrive.
-    if (!stopped) {
+    // With a work-sharing word the consumers do not know their item count:
+    // tell them that no item follows with a header of kind kDoneItem in the
+    // next stage, its phase completed by a plain arrive.
+    if (sc.word && !stopped) {
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round == 0 || mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
@@ -601,10 +631,14 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     return;
   }
 
-  // Consumers: the items come in stage order until an end marker.
+  // Consumers: the items come in stage order.  In the fixed order CTA b's
+  // items are b, b + G, ... below n; a launch that shares items ends each
+  // CTA's stream with an end marker instead.
   wait_for_previous_grid();
   const int ct = (int)threadIdx.x - 32;
-  for (int64_t k = 0;; ++k) {
+  const bool counted = a.sched.word == nullptr;
+  int64_t i = blockIdx.x;
+  for (int64_t k = 0; !counted || i < a.n_items; ++k, i += gridDim.x) {
     const int s = (int)(k % kStages);
     if (!mbar_wait(&full[s], (uint32_t)(k / kStages) & 1u, a.wait_limit_ns)) {
       if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
@@ -663,6 +697,7 @@ Sched make_sched(unsigned long long *word, std::atomic<uint32_t> *epoch, int64_t
     rounds = (n / grid) * 3 / 4;
   }
   if (n - rounds * grid > kSharedMaxItems) rounds = (n - kSharedMaxItems + grid - 1) / grid;
+  if (rounds < 1) rounds = 1;  // every CTA's first item comes in the fixed order
   sc.word = word;
   sc.fixed_rounds = rounds;
   sc.tag = epoch->fetch_add(1, std::memory_order_relaxed) % 0xFFFFFFu + 1u;

@@ -389,7 +389,8 @@ void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns);
  *   FSDP_SCHEDULE_FIXED    every launch keeps the fixed order: block b takes
  *                          items b, b + G, b + 2G, ... of its G blocks.
  *   FSDP_SCHEDULE_SHARED   every launch with a device table hands out all its
- *                          items through the word, at any size.
+ *                          items but each block's first through the word, at
+ *                          any size.
  *   FSDP_SCHEDULE_MIXED    as FSDP_SCHEDULE_SHARED, but blocks with an odd
  *                          index act as if another launch held the word.
  * Returns FSDP_EINVAL (and changes nothing) for any other mode.

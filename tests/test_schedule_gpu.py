@@ -5,8 +5,8 @@ A launch hands out its work items in a fixed order (block b takes items b,
 b + G, ...) or, for its last items, to whichever block asks first through a
 work-sharing word in the layout's device memory.  The bytes written must not
 depend on that choice, so every entry point is checked bit-exactly in each
-schedule the test hook offers: the fixed order, every item through the word,
-and a mix in which odd blocks keep the fixed order while even blocks share
+schedule the test hook offers: the fixed order, every item but each block's
+first through the word, and a mix in which odd blocks keep the fixed order while even blocks share
 the word (some items are then written twice, with the same bytes).  Then
 launches of one layout that overlap on the GPU, on two streams, must each
 give the oracle's bytes: the word is held by one launch at a time and the
