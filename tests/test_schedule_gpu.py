@@ -120,3 +120,41 @@ def test_overlapping_launches_on_two_streams(fp, schedule, mode):
                     assert torch.equal(got, want), f"stream {k} round {it}: copy-out param {p} differs"
     finally:
         L.close()
+
+
+@pytest.mark.parametrize("mode", ["DEFAULT", "SHARED", "MIXED"])
+def test_batched_and_single_launches_share_one_word(fp, schedule, mode):
+    """A batched pack of [L, L] takes its work-sharing word from its first
+    layout, the same word a single pack of L uses.  Batched packs on one
+    stream and single packs on another, issued alternately, must each give
+    the oracle's bytes whichever launch holds the word."""
+    schedule(getattr(fp, f"FSDP_SCHEDULE_{mode}"))
+    work = wl.mixed_50m(W=8, layers=2)
+    specs, W = work.groups[0], work.W
+    pl = oracle.plan(oracle.params_from_specs(specs), W)
+    grads_h = [wl.grad_values(work, 0, i, specials=0.01) for i in range(len(specs))]
+    want = oracle.pack_reduce_scatter(pl, grads_h)
+    L = fp.fsdp_plan_layout(specs, W)
+    try:
+        if mode == "DEFAULT":
+            # Twice the layout's items reach the sharing threshold of a batch of two.
+            assert 2 * fp.fsdp_layout_query(L).pack_items >= 8 * 2 * 152 * 3
+        grads = [_upload(g) for g in grads_h]
+        want_d = [_upload(x) for x in want]
+        s_batched, s_single = torch.cuda.Stream(), torch.cuda.Stream()
+        rounds = 6
+        batched = [[torch.full_like(x, 0x5A) for _ in range(2) for x in want_d] for _ in range(rounds)]
+        single = [[torch.full_like(x, 0xA5) for x in want_d] for _ in range(rounds)]
+        torch.cuda.synchronize()
+        for it in range(rounds):
+            fp.fsdp_pack_reduce_scatter_batched([L, L], grads + grads, batched[it], stream=s_batched)
+            fp.fsdp_pack_reduce_scatter(L, grads, single[it], stream=s_single)
+        torch.cuda.synchronize()
+        fp.fsdp_sync_status(L)
+        for it in range(rounds):
+            for b, got in enumerate(batched[it]):
+                assert torch.equal(got, want_d[b % len(want_d)]), f"round {it}: batched bucket {b} differs"
+            for b, got in enumerate(single[it]):
+                assert torch.equal(got, want_d[b]), f"round {it}: single bucket {b} differs"
+    finally:
+        L.close()
