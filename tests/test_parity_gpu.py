@@ -151,6 +151,57 @@ def test_kda_block_full_size(fp, W, reduce):
         run.close()
 
 
+@pytest.mark.parametrize("reduce", ["f32", "bf16"])
+def test_kda_eight_blocks_batched_full_size(fp, reduce):
+    """The whole 1.75B-parameter KDA-style layout at W = 8, one fully_shard
+    group per block, packed in one batched launch as the benchmark's
+    eight-block run does: 3.5 GB of gradients into 7 GB (FP32) or 3.5 GB
+    (BF16) of bucket rows.  The gradients are seeded random bit patterns, so
+    NaN payloads, infinities and subnormals pass through every cast.  Each
+    bucket is checked on random elements plus every run's edges, computed one
+    by one by the oracle.  The pack runs twice, into buffers pre-filled with
+    two different bytes, and the two results must be equal: every output byte
+    was written."""
+    W, blocks = 8, 8
+    work = wl.kda_block(W=W, reduce=reduce, blocks=blocks)
+    assert len(work.groups) == blocks
+    layouts, plans, grads_d, grads_h, outs = [], [], [], [], []
+    try:
+        for g, specs in enumerate(work.groups):
+            plans.append(oracle.plan(oracle.params_from_specs(specs), W))
+            layouts.append(fp.fsdp_plan_layout(specs, W))
+            row_d, row_h = [], []
+            for i, s in enumerate(specs):
+                t = wl.device_random_bytes(s.numel * ESZ[s.grad_dtype], 9100, g, i)
+                row_d.append(t)
+                row_h.append(t.cpu().numpy().view(NP[s.grad_dtype]))
+            grads_d.append(row_d)
+            grads_h.append(row_h)
+        names = [["f32" if d == oracle.F32 else "bf16" for d in pl.bucket_dtype] for pl in plans]
+        flat_grads = [t for row in grads_d for t in row]
+        for fill in (0xA5, 0x5A):
+            bufs = [[torch.full((W * S * ESZ[n],), fill, dtype=torch.uint8, device="cuda")
+                     for n, S in zip(nm, pl.bucket_S)] for nm, pl in zip(names, plans)]
+            fp.fsdp_pack_reduce_scatter_batched(layouts, flat_grads, [b for row in bufs for b in row])
+            fp.fsdp_sync_status(layouts[0])
+            outs.append(bufs)
+        for g in range(blocks):
+            for b, (x, y) in enumerate(zip(*(o[g] for o in outs))):
+                assert torch.equal(x, y), f"block {g} bucket {b}: bytes left unwritten"
+        del outs[1]
+        rng = np.random.default_rng(9100)
+        for g in range(blocks):
+            for b, (buf, n) in enumerate(zip(outs[0][g], names[g])):
+                idx = _sample_indices(plans[g], b, rng, 250_000)
+                view = buf.view(torch.int32 if n == "f32" else torch.int16)
+                got = view[torch.from_numpy(idx).cuda()].cpu().numpy().view(NP[n])
+                want = oracle.pack_samples(plans[g], grads_h[g], b, idx)
+                assert np.array_equal(got, want), f"block {g} bucket {b}: {first_mismatch(got, want)}"
+    finally:
+        for L in layouts:
+            L.close()
+
+
 def test_many_parameters_use_the_larger_parameter_blocks(fp):
     rnd = np.random.default_rng(5)
     for n in (70, 600, 4000):
