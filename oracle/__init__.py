@@ -223,6 +223,26 @@ def _check(arr, dt, n, what):
                          f"got {arr.size} {arr.dtype}")
 
 
+def _check_plan(pl: Plan) -> None:
+    """Refuse a plan whose offsets would reach outside the buffers the C loops
+    are given (they trust the plan).  Only bounds are checked here; the
+    offsets' values are what the pins check."""
+    P = len(pl.params)
+    if any(len(x) != P for x in (pl.chunk, pl.bucket_of, pl.bucket_off, pl.group_of, pl.group_elem_off)) \
+            or len(pl.bucket_S) != len(pl.bucket_dtype) or len(pl.group_byte_off) != len(pl.group_pair) \
+            or len(pl.group_elems) != len(pl.group_pair):
+        raise ValueError("plan: list lengths disagree")
+    for p, prm in enumerate(pl.params):
+        c, b, g = pl.chunk[p], pl.bucket_of[p], pl.group_of[p]
+        if c < 0 or not 0 <= b < len(pl.bucket_S) or not 0 <= g < len(pl.group_pair):
+            raise ValueError(f"plan: parameter {p} has a negative chunk or no bucket / group")
+        if pl.bucket_off[p] < 0 or pl.bucket_off[p] + c > pl.bucket_S[b]:
+            raise ValueError(f"plan: parameter {p} does not fit its bucket row")
+        end = pl.group_byte_off[g] + (pl.group_elem_off[p] + c) * DTYPE_SIZE[prm.param_dtype]
+        if pl.group_elem_off[p] < 0 or pl.group_byte_off[g] < 0 or end > pl.S_ag:
+            raise ValueError(f"plan: parameter {p} does not fit the all-gather row")
+
+
 def f32_to_bf16(bits: np.ndarray) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint32)
     out = np.empty(bits.shape, np.uint16)
@@ -239,11 +259,14 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
 
 def pack_reduce_scatter(pl: Plan, grads, out=None):
     """Reduce-scatter copy-in: one [W * S_b] buffer per bucket (flat, row r at r*S_b)."""
+    _check_plan(pl)
     grads = [np.ascontiguousarray(g).reshape(-1) for g in grads]
     for p, g in zip(pl.params, grads):
         _check(g, p.grad_dtype, p.numel, "grad")
     if out is None:
         out = [np.empty(pl.W * S, DTYPE_NP[dt]) for dt, S in zip(pl.bucket_dtype, pl.bucket_S)]
+    for o, dt, S in zip(out, pl.bucket_dtype, pl.bucket_S):
+        _check(o, dt, pl.W * S, "bucket buffer")
     keep = [_i64([p.numel for p in pl.params]), _i32([p.grad_dtype for p in pl.params]),
             _i64(pl.chunk), _i32(pl.bucket_of), _i64(pl.bucket_off),
             _i32(pl.bucket_dtype), _i64(pl.bucket_S)]
@@ -255,8 +278,13 @@ def pack_reduce_scatter(pl: Plan, grads, out=None):
 
 def pack_samples(pl: Plan, grads, b: int, idx: np.ndarray) -> np.ndarray:
     """Elements idx (flat indices into bucket b's [W * S_b] buffer), one by one."""
+    _check_plan(pl)
     grads = [np.ascontiguousarray(g).reshape(-1) for g in grads]
+    for p, g in zip(pl.params, grads):
+        _check(g, p.grad_dtype, p.numel, "grad")
     idx = _i64(idx)
+    if idx.size and (idx.min() < 0 or idx.max() >= pl.W * pl.bucket_S[b]):
+        raise ValueError("sample index outside the bucket")
     out = np.empty(idx.size, DTYPE_NP[pl.bucket_dtype[b]])
     keep = [_i64([p.numel for p in pl.params]), _i32([p.grad_dtype for p in pl.params]),
             _i64(pl.chunk), _i32(pl.bucket_of), _i64(pl.bucket_off)]
@@ -268,11 +296,14 @@ def pack_samples(pl: Plan, grads, b: int, idx: np.ndarray) -> np.ndarray:
 
 def allgather_copy_in(pl: Plan, shards, out=None) -> np.ndarray:
     """All-gather copy-in of one rank: S_ag bytes."""
+    _check_plan(pl)
     shards = [np.ascontiguousarray(s).reshape(-1) for s in shards]
     for p, c, s in zip(pl.params, pl.chunk, shards):
         _check(s, p.shard_dtype, c, "shard")
     if out is None:
         out = np.empty(pl.S_ag, np.uint8)
+    if out.dtype != np.uint8 or not out.flags.c_contiguous or out.size != pl.S_ag:
+        raise ValueError("all-gather input must be S_ag contiguous bytes")
     keep = [_i64(pl.chunk), _i32([p.shard_dtype for p in pl.params]),
             _i32([p.param_dtype for p in pl.params]), _i32(pl.group_of),
             _i64(pl.group_elem_off), _i64(pl.group_byte_off)]
@@ -284,11 +315,14 @@ def allgather_copy_in(pl: Plan, shards, out=None) -> np.ndarray:
 
 def allgather_copy_out(pl: Plan, ag_out: np.ndarray, out=None):
     """All-gather copy-out: the gathered [W * S_ag] bytes back to full parameters."""
+    _check_plan(pl)
     ag_out = np.ascontiguousarray(ag_out, dtype=np.uint8).reshape(-1)
     if ag_out.size != pl.W * pl.S_ag:
         raise ValueError("gathered buffer must hold W * S_ag bytes")
     if out is None:
         out = [np.empty(p.numel, DTYPE_NP[p.param_dtype]) for p in pl.params]
+    for o, p in zip(out, pl.params):
+        _check(o, p.param_dtype, p.numel, "full parameter")
     keep = [_i64([p.numel for p in pl.params]), _i64(pl.chunk),
             _i32([p.param_dtype for p in pl.params]), _i32(pl.group_of),
             _i64(pl.group_elem_off), _i64(pl.group_byte_off)]
@@ -310,11 +344,14 @@ def params_from_specs(specs):
 def reduce_scatter_copy_out(pl: Plan, rows, out=None):
     """This rank's reduced bucket rows (S_b elements each) -> per-parameter
     sharded gradients (c_p elements of the shard dtype)."""
+    _check_plan(pl)
     rows = [np.ascontiguousarray(r).reshape(-1) for r in rows]
     for b, (dt, S) in enumerate(zip(pl.bucket_dtype, pl.bucket_S)):
         _check(rows[b], dt, S, "reduced row")
     if out is None:
         out = [np.empty(c, DTYPE_NP[p.shard_dtype]) for p, c in zip(pl.params, pl.chunk)]
+    for o, p, c in zip(out, pl.params, pl.chunk):
+        _check(o, p.shard_dtype, c, "sharded gradient")
     keep = [_i64(pl.chunk), _i32(pl.bucket_of), _i64(pl.bucket_off), _i32(pl.bucket_dtype),
             _i32([p.shard_dtype for p in pl.params])]
     _load().oracle_reduce_scatter_copy_out(len(pl.params), *(a.ctypes.data for a in keep), _ptrs(rows), _ptrs(out))

@@ -5,6 +5,9 @@ wrong comparison, a lost bit) in a temporary copy of ``oracle/fsdp_oracle.c``,
 builds it, swaps it in for the real oracle library, and re-runs the pins of
 tests/test_oracle_pins.py.  The mutants run in this process, so every one of
 them keeps all its memory accesses inside the buffers it is given.  At least one pin must fail for every mutant.
+The planner mutants at the end do the same with the oracle's Python planner;
+the oracle's wrappers refuse a plan whose offsets do not fit their buffers,
+so a broken plan cannot make the C loops write out of bounds.
 Everything runs on the CPU; the mistakes are planted in the oracle only.
 """
 import ctypes
@@ -96,3 +99,62 @@ def test_pins_catch_mutant(name, tmp_path):
     finally:
         oracle._lib = saved
     assert failed, f"no pin caught mutant {name!r}"
+
+
+# Mistakes planted in the oracle's planner (Python).  A mutated copy of
+# oracle.plan is compiled from its source in the oracle module's namespace and
+# put in place of the real one, both in the oracle module and where the pins
+# imported it by name.
+PLAN_MUTANTS = {
+    "plan: chunk rounded down":
+        ("c = _ceil_div(p.numel, W)", "c = p.numel // W"),
+    "plan: row chunk counted in elements, not rows":
+        ("c = _ceil_div(p.numel // rows_of, W) * rows_of", "c = _ceil_div(p.numel, W)"),
+    "plan: bucket offset counts every earlier parameter":
+        ("pl.bucket_off.append(pl.bucket_S[b])", "pl.bucket_off.append(sum(pl.chunk[:-1]))"),
+    "plan: buckets keyed by grad dtype":
+        ("if p.reduce_dtype not in bucket_index:\n"
+         "            bucket_index[p.reduce_dtype] = len(pl.bucket_dtype)\n"
+         "            pl.bucket_dtype.append(p.reduce_dtype)\n"
+         "            pl.bucket_S.append(0)\n"
+         "        b = bucket_index[p.reduce_dtype]",
+         "if p.grad_dtype not in bucket_index:\n"
+         "            bucket_index[p.grad_dtype] = len(pl.bucket_dtype)\n"
+         "            pl.bucket_dtype.append(p.grad_dtype)\n"
+         "            pl.bucket_S.append(0)\n"
+         "        b = bucket_index[p.grad_dtype]"),
+    "plan: group element offset counts every earlier group":
+        ("pl.group_elem_off.append(pl.group_elems[g])", "pl.group_elem_off.append(sum(pl.group_elems))"),
+    "plan: groups keyed by param dtype only":
+        ("pair = (p.shard_dtype, p.param_dtype)", "pair = (p.param_dtype, p.param_dtype)"),
+    "plan: group starts not aligned":
+        ("start = _align16(end)", "start = end"),
+    "plan: all-gather row not rounded up":
+        ("pl.S_ag = _align16(end)", "pl.S_ag = end"),
+    "plan: group byte size taken as FP32":
+        ("end = start + pl.group_elems[g] * DTYPE_SIZE[pi]", "end = start + pl.group_elems[g] * 4"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLAN_MUTANTS))
+def test_pins_catch_planner_mutant(name):
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle.plan))
+    old, new = PLAN_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name!r} not found exactly once"
+    namespace = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "<mutant plan>", "exec"), namespace)
+    real = oracle.plan
+    oracle.plan = pins.plan = namespace["plan"]
+    failed = []
+    try:
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failed.append(pin.__name__)
+                break
+    finally:
+        oracle.plan = pins.plan = real
+    assert failed, f"no pin caught planner mutant {name!r}"
