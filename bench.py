@@ -9,22 +9,29 @@ x 2 per layer (8,192 elements); reduce dtype FP32; local shards FP32; param
 dtype BF16 for the matrices and FP32 for the norms.  Values are seeded
 N(0, 1) draws (synthetic: no dataset or trained weights exist for this).
 
-One step is one pass of the whole hot path for that group on one GPU:
-  1. reduce-scatter copy-in: pack every gradient into the [8, 6,292,480] FP32
-     buffer (cast in flight, padding zeroed);
-  2. all-gather copy-in of this rank's shards into its row of the gathered
-     buffer (the other rows stand for what the all-gather brings in);
-  3. all-gather copy-out of the gathered [8, S_ag] buffer into full params.
+The metric is the reduce-scatter pack of that group, the step the news
+item times in isolation: gradients -> the [8, 6,292,480] FP32 buffer, cast
+in flight, padding zeroed.  The timed region is K packs back to back on one
+stream, alternating two buffer sets (each larger than L2), with no event or
+host synchronisation between launches; `value` is the pack's algorithmic
+bytes over that time and `ms_per_step` the time of one pack.  Also reported:
+  * hot_path_step: the whole path per group -- pack, all-gather copy-in of one
+    rank (the other rows stand for what the all-gather brings in), all-gather
+    copy-out -- timed the same way;
+  * ops: per-operation device times from a pass with CUDA events around
+    every launch (events serialise the launches);
+  * roofline of the pack against the measured copy bandwidth and against a
+    plain 1:2 streaming widen of the same bytes run in the same process;
+  * e2e: the pack through the same C-ABI call with pinned host buffers (the
+    gradients uploaded and the bucket downloaded every step);
+  * extra_workloads: the ~500-parameter transformer layout (24 groups, one
+    launch per operation) and one KDA-style block at W = 64;
+  * cpu_baseline: the CPU oracle's pack on a bounded sample.
 Nothing is communicated: W is a layout parameter.  With --gpus N (launched
-by torchrun) every rank runs the same step on its own GPU with no collective
+by torchrun) every rank runs the same work on its own GPU with no collective
 on the data path ("replicas"); the timing is the max over ranks.
-
-Reported (one JSON line on rank 0): value = algorithmic bytes of all ranks'
-steps / time (GB/s), per-operation device times from CUDA events, the
-roofline of the dominant kernel (the pack), the SM clocks sampled during the
-timed region, an end-to-end figure through the same API with host buffers,
-and the CPU oracle timed on a bounded sample.  --impl reference times the
-CPU oracle alone on bounded samples of the same workload.
+--impl reference times the CPU oracle's pack alone on bounded samples of the
+same workload.
 
 Algorithmic bytes (reads count valid source elements, writes count every
 destination slot including padding and alignment gaps):
@@ -60,7 +67,7 @@ NOMINAL_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the metric is quoted again
 FALLBACK_HBM_GBS = 6800.0  # used only when no measured copy bandwidth is available
 CHUNKING = {False: "flattened: c_p = ceil(n_p / W)", True: "dim-0 rows: c_p = ceil(d0 / W) * row elements"}
 ESZ = {"f32": 4, "bf16": 2}
-STEP = "step = per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
+STEP = "per group: reduce-scatter pack + all-gather copy-in (one rank) + all-gather copy-out"
 STEP_RS = " + reduce-scatter copy-out (row 0 of each bucket as this rank's reduced row)"
 STEP_ERS = " + emulated reduce-scatter after the pack (this rank's buckets + W-1 other ranks' buffers)"
 WORKLOADS = {
@@ -90,7 +97,9 @@ WORKLOADS = {
                     "kda_block_W8_two_buckets: one KDA-style block, W=8, reduce dtype = gradient dtype "
                     "(BF16 and FP32 buckets)"),
 }
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pack_mixed50m_w8_ncu.md")
+# Counters of one ncu capture of the pack on mixed50m (written by hand from the
+# capture; see the .md summary of the same name for the command and the reading).
+PROFILE_COUNTERS = os.path.join(ROOT, "profiles", "pack_mixed50m_w8_ncu.json")
 
 
 def parse_args(argv=None):
@@ -115,9 +124,15 @@ def parse_args(argv=None):
     ap.add_argument("--row-chunks", action="store_true",
                     help="plan every parameter by dim-0 rows (c_p = ceil(d0 / W) rows) instead of flattened")
     ap.add_argument("--graph", action="store_true",
-                    help="time the step as replays of a CUDA graph holding two steps (both buffer sets)")
+                    help="time packs and steps as replays of CUDA graphs holding two of each (both buffer sets)")
     ap.add_argument("--batched", action="store_true",
                     help="one launch per operation for all of the workload's groups (*_batched entry points)")
+    ap.add_argument("--evented-steps", type=int, default=2000,
+                    help="whole steps of the pass with CUDA events around every launch (per-operation times)")
+    ap.add_argument("--reference-iters", type=int, default=400,
+                    help="iterations of the same-run plain copies of the pack's bytes (0 = skip)")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="skip the extra workloads (transformer layout batched, one KDA block at W = 64)")
     return ap.parse_args(argv)
 
 
@@ -208,24 +223,22 @@ def kernel_source_hash() -> str:
 
 
 def read_traffic():
-    """DRAM bytes per pack launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+    """DRAM and L2 write bytes of one pack launch from the committed ncu
+    counters, if they were taken on the current kernel source (else None)."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(PROFILE_COUNTERS) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
         return None
-    fields = {}
-    for line in text.splitlines():
-        line = line.strip().strip("`")
-        if ":" in line:
-            k, v = line.split(":", 1)
-            fields[k.strip()] = v.strip()
-    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     try:
-        return int(fields["dram_bytes_per_pack_launch"])
-    except (KeyError, ValueError):
+        rd, wr = int(d["dram__bytes_read.sum"]), int(d["dram__bytes_write.sum"])
+        l2w = int(d["lts__t_sectors_srcunit_tex_op_write.sum"]) * 32
+    except (KeyError, ValueError, TypeError):
         return None
+    return {"traffic": rd + wr, "traffic_dram_read": rd, "traffic_dram_write": wr, "traffic_l2_write": l2w,
+            "traffic_source": os.path.relpath(PROFILE_COUNTERS, ROOT)}
 
 
 # ---------------------------------------------------------------------------
@@ -284,7 +297,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# Host inputs (seeded), packed into flat byte buffers with aligned offsets.
+# Inputs (seeded), packed into flat byte buffers with aligned offsets.
 # ---------------------------------------------------------------------------
 def flat_offsets(sizes, align=256):
     offs, at = [], 0
@@ -295,7 +308,7 @@ def flat_offsets(sizes, align=256):
 
 
 def host_inputs(work, g, rows=False):
-    """Seeded gradients and every rank's shards of group g."""
+    """Seeded gradients and every rank's shards of group g (host arrays)."""
     specs, W = work.groups[g], work.W
     c = chunks(specs, W, rows)
     grads = [wl.grad_values(work, g, i) for i in range(len(specs))]
@@ -304,7 +317,32 @@ def host_inputs(work, g, rows=False):
     return grads, shards
 
 
-def flatten(arrays, offs, total):
+def device_inputs(work, g, rows=False):
+    """The same inputs drawn on the device (torch's seeded generator, the same
+    distributions), for workloads too large to draw on the host quickly."""
+    specs, W = work.groups[g], work.W
+    c = chunks(specs, W, rows)
+    grads = [wl.device_normal_bits(s.numel, s.grad_dtype, work.std, work.seed, g, i, 1) for i, s in enumerate(specs)]
+    shards = []
+    for r in range(W):
+        row = []
+        for i, s in enumerate(specs):
+            t = wl.device_normal_bits(c[i], s.shard_dtype, work.std, work.seed, g, i, 3, r)
+            valid = max(0, min(c[i], s.numel - r * c[i]))
+            t[valid * ESZ[s.shard_dtype]:] = 0
+            row.append(t)
+        shards.append(row)
+    return grads, shards
+
+
+def flatten(arrays, offs, total, torch=None):
+    """Concatenate per-parameter byte arrays at the given offsets: numpy arrays
+    into a host buffer, device tensors into a device buffer."""
+    if arrays and torch is not None and isinstance(arrays[0], torch.Tensor):
+        out = torch.zeros(total, dtype=torch.uint8, device=arrays[0].device)
+        for a, o in zip(arrays, offs):
+            out[o:o + a.numel()].copy_(a)
+        return out
     out = np.zeros(total, np.uint8)
     for a, o in zip(arrays, offs):
         b = a.view(np.uint8)
@@ -312,29 +350,29 @@ def flatten(arrays, offs, total):
     return out
 
 
+def to_device(flat, torch):
+    return flat if isinstance(flat, torch.Tensor) else torch.from_numpy(flat).to("cuda")
+
+
 # ---------------------------------------------------------------------------
-# The CPU oracle on bounded samples: one (rank, parameter) run at a time.
+# The CPU oracle's pack on bounded samples: one (rank, parameter) run at a time.
 # ---------------------------------------------------------------------------
 class OracleSampler:
-    """Cycles through the segments of one step of the path over every group
-    (pack runs, copy-in runs of rank 0, copy-out runs), each with its
-    algorithmic bytes."""
+    """Cycles through the runs of the reduce-scatter pack of every group --
+    one (bucket, rank, parameter) run at a time, each with its algorithmic
+    bytes -- on the oracle."""
 
     def __init__(self, work, inputs, rows=False):
         import oracle
         self.oracle = oracle
         W = work.W
         self.segs = []
+        self.pack_bytes = 0
         for g, specs in enumerate(work.groups):
-            grads, shards = inputs[g]
+            grads = inputs[g][0]
             pl = oracle.plan(oracle.params_from_specs(specs), W, row_elems=row_elems(specs) if rows else None)
-            st = {
-                "pl": pl, "grads": grads, "shards0": shards[0],
-                "bufs": [np.empty(W * S, oracle.DTYPE_NP[d]) for d, S in zip(pl.bucket_dtype, pl.bucket_S)],
-                "row": np.empty(pl.S_ag, np.uint8),
-                "gathered": np.concatenate([oracle.allgather_copy_in(pl, shards[r]) for r in range(W)]),
-                "full": [np.empty(p.numel, oracle.DTYPE_NP[p.param_dtype]) for p in pl.params],
-            }
+            st = {"pl": pl, "grads": grads,
+                  "bufs": [np.empty(W * S, oracle.DTYPE_NP[d]) for d, S in zip(pl.bucket_dtype, pl.bucket_S)]}
             sz = oracle.DTYPE_SIZE
             for b in range(len(pl.bucket_dtype)):
                 for r in range(W):
@@ -343,34 +381,15 @@ class OracleSampler:
                             continue
                         valid = max(0, min(pl.chunk[p], prm.numel - r * pl.chunk[p]))
                         nbytes = valid * sz[prm.grad_dtype] + pl.chunk[p] * sz[pl.bucket_dtype[b]]
-                        self.segs.append((self._pack, (st, r, p), nbytes))
-            gap = pl.S_ag - sum(c * sz[p.param_dtype] for c, p in zip(pl.chunk, pl.params))
-            self.segs.append((self._clear, (st,), gap))
-            for p, prm in enumerate(pl.params):
-                self.segs.append((self._copy_in, (st, p), pl.chunk[p] * (sz[prm.shard_dtype] + sz[prm.param_dtype])))
-            for p, prm in enumerate(pl.params):
-                for r in range(W):
-                    valid = max(0, min(pl.chunk[p], prm.numel - r * pl.chunk[p]))
-                    self.segs.append((self._copy_out, (st, p, r), 2 * valid * sz[prm.param_dtype]))
-        self.step_bytes = sum(s[2] for s in self.segs)
+                        self.segs.append((st, r, p, nbytes))
+            self.pack_bytes += (sum(prm.numel * sz[prm.grad_dtype] for prm in pl.params)
+                                + sum(W * S * sz[d] for d, S in zip(pl.bucket_dtype, pl.bucket_S)))
         self.i = 0
 
-    def _pack(self, st, r, p):
-        self.oracle.pack_segment(st["pl"], st["grads"], st["bufs"], r, p)
-
-    def _clear(self, st):
-        self.oracle.allgather_copy_in_clear(st["pl"], st["row"])
-
-    def _copy_in(self, st, p):
-        self.oracle.allgather_copy_in_segment(st["pl"], st["shards0"], st["row"], p)
-
-    def _copy_out(self, st, p, r):
-        self.oracle.allgather_copy_out_segment(st["pl"], st["gathered"], st["full"], p, r)
-
     def next(self) -> int:
-        fn, args, nbytes = self.segs[self.i]
+        st, r, p, nbytes = self.segs[self.i]
         self.i = (self.i + 1) % len(self.segs)
-        fn(*args)
+        self.oracle.pack_segment(st["pl"], st["grads"], st["bufs"], r, p)
         return nbytes
 
 
@@ -395,19 +414,29 @@ def host_cpu() -> dict:
 
 
 def cpu_baseline(sampler: OracleSampler, seconds: float) -> dict:
-    """Whole steps of the oracle (all segments in order) for about `seconds`."""
-    done_bytes, steps = 0, 0
+    """The oracle's pack, run after run, for about `seconds`."""
+    done_bytes, runs = 0, 0
     t0 = time.perf_counter()
-    while True:
-        for _ in range(len(sampler.segs)):
-            done_bytes += sampler.next()
-        steps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
+    while time.perf_counter() - t0 < seconds or runs == 0:
+        done_bytes += sampler.next()
+        runs += 1
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{steps} whole step(s) of the same workload (pack, copy-in of one rank, copy-out), "
-                      f"single-threaded C oracle, {dt:.1f} s", **host_cpu()}
+            "sample": f"{runs} (bucket, rank, parameter) runs of the reduce-scatter pack of the same workload "
+                      f"({done_bytes / sampler.pack_bytes:.2f} whole packs), single-threaded C oracle, {dt:.1f} s",
+            **host_cpu()}
+
+
+def make_config(args, work, description, n_groups, n_launch, pack_bytes, world):
+    """The `config` of both arms' JSON lines (identical for the same flags)."""
+    return {"workload": f"{description}; timed: the reduce-scatter pack of every group, launches back to back",
+            "world_size_layout": work.W, "chunking": CHUNKING[args.row_chunks], "groups": n_groups,
+            "launches_per_op": n_launch, "pack_bytes": pack_bytes,
+            "launch": ("CUDA graph of two packs, replayed" if args.graph
+                       else "stream launches from the host") + (", batched over groups" if args.batched else ""),
+            "parallelism": f"replicas x{world} (no data-path collective)",
+            "l2": f"inputs larger than L2: two rotating buffer sets of {2 * pack_bytes / 1e9:.2f} GB of pack "
+                  "traffic vs 129 MB L2; no flush"}
 
 
 # ---------------------------------------------------------------------------
@@ -416,13 +445,13 @@ def cpu_baseline(sampler: OracleSampler, seconds: float) -> dict:
 class DeviceSet:
     """One complete set of device buffers for a step (two sets rotate)."""
 
-    def __init__(self, fp, torch, L, specs, W, info, host_grads, host_shards, rank_row, others=None, rows=False):
+    def __init__(self, fp, torch, L, specs, W, info, grads, shards, rank_row, others=None, rows=False):
         dev = torch.device("cuda")
         c = chunks(specs, W, rows)
         self.S_ag = info.ag_bytes
         g_sizes = [s.numel * ESZ[s.grad_dtype] for s in specs]
         goffs, gtot = flat_offsets(g_sizes)
-        self.grads = torch.from_numpy(flatten(host_grads, goffs, gtot)).to(dev)
+        self.grads = to_device(flatten(grads, goffs, gtot, torch), torch)
         self.grad_ptrs = fp.pointer_array([self.grads.data_ptr() + o for o in goffs])
         self.buckets = [torch.empty(fp.fsdp_layout_bucket(L, b).bytes, dtype=torch.uint8, device=dev)
                         for b in range(info.n_buckets)]
@@ -430,7 +459,7 @@ class DeviceSet:
         s_sizes = [ci * ESZ[s.shard_dtype] for ci, s in zip(c, specs)]
         soffs, stot = flat_offsets(s_sizes)
         self.shard_offs, self.shard_tot = soffs, stot
-        self.shards = torch.from_numpy(flatten(host_shards[rank_row], soffs, stot)).to(dev)
+        self.shards = to_device(flatten(shards[rank_row], soffs, stot, torch), torch)
         self.shard_ptrs = fp.pointer_array([self.shards.data_ptr() + o for o in soffs])
         self.gathered = torch.empty(W * self.S_ag, dtype=torch.uint8, device=dev)
         self.row_ptr = self.gathered.data_ptr() + rank_row * self.S_ag
@@ -459,11 +488,14 @@ class DeviceSet:
         for r in range(W):
             if r == rank_row:
                 continue
-            other = torch.from_numpy(flatten(host_shards[r], soffs, stot)).to(dev)
+            other = to_device(flatten(shards[r], soffs, stot, torch), torch)
             fp.fsdp_allgather_copy_in(L, [other.data_ptr() + o for o in soffs],
                                       self.gathered.data_ptr() + r * self.S_ag)
             torch.cuda.synchronize()
             del other
+
+    def pack(self, fp, L, h):
+        fp.fsdp_pack_reduce_scatter(L, self.grad_ptrs, self.bucket_ptrs, h)
 
     def step(self, fp, L, h, ev=None, rs=False):
         """pack, [emulated reduce-scatter], copy-in, copy-out, [rs copy-out];
@@ -525,6 +557,10 @@ class Batch:
                 gathered=fp.pointer_array([s.gathered.data_ptr() for s in ss]), full=cat(s.full_ptrs for s in ss),
                 row0=cat(s.row0_ptrs for s in ss), sharded=cat(s.sharded_ptrs for s in ss)))
 
+    def pack(self, fp, h, k):
+        a = self.sets[k]
+        fp.fsdp_pack_reduce_scatter_batched(self.layouts, a["grads"], a["buckets"], h)
+
     def step(self, fp, h, k, ev=None, rs=False):
         a = self.sets[k]
         if ev is not None:
@@ -585,19 +621,7 @@ def precast_comparison(fp, torch, work, grp, h, iters, rows=False):
             a = args[k & 1]
             fp.fsdp_pack_reduce_scatter(grp.L, a[4], a[3], h)
 
-        def loop(fn):
-            for k in range(10):
-                fn(k)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            e0.record()
-            for k in range(iters):
-                fn(k)
-            e1.record()
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / iters
-
-        pre_ms, fused_ms = loop(precast), loop(fused)
+        pre_ms, fused_ms = loop_ms(torch, precast, iters), loop_ms(torch, fused, iters)
         for L in (L_cast, L32, grp.L):
             fp.fsdp_sync_status(L)
         bucket_bytes = [fp.fsdp_layout_bucket(L32, b).bytes for b in range(fp.fsdp_layout_query(L32).n_buckets)]
@@ -611,6 +635,50 @@ def precast_comparison(fp, torch, work, grp, h, iters, rows=False):
             "precast_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9, "launches": 2 * iters + iters}
 
 
+def loop_ms(torch, fn, iters, warm=10):
+    """Mean ms per call of fn(k), k = 0 .. iters - 1, timed back to back with
+    CUDA events on the current stream after `warm` untimed calls."""
+    for k in range(warm):
+        fn(k)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for k in range(iters):
+        fn(k)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def same_run_references(fp, torch, pack_bytes, iters):
+    """Plain copies of the pack's byte count in the same process and loop
+    style: the library's streaming BF16 -> FP32 widen (the pack's 1 : 2 mix of
+    bytes read to bytes written) and torch's 1 : 1 device copy."""
+    n = pack_bytes // 6 // 8 * 8          # BF16 elements: 2n read + 4n written
+    src = [torch.empty(2 * n, dtype=torch.uint8, device="cuda").random_(0, 256) for _ in range(2)]
+    dst = [torch.empty(4 * n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    widen_ms = loop_ms(torch, lambda k: fp.fsdp_debug_stream_widen(src[k & 1], n, dst[k & 1]), iters)
+    half = pack_bytes // 2 // 16 * 16
+    a = [torch.empty(half, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    b = [torch.empty(half, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    copy_ms = loop_ms(torch, lambda k: b[k & 1].copy_(a[k & 1]), iters)
+    del src, dst, a, b
+    return {"plain_widen_1to2": {"what": "fsdp_debug_stream_widen, BF16 -> FP32, same bytes",
+                                 "bytes": 6 * n, "us": widen_ms * 1e3, "gbs": 6 * n / (widen_ms * 1e-3) / 1e9},
+            "copy_1to1": {"what": "torch copy_ of uint8, half the bytes read and half written",
+                          "bytes": 2 * half, "us": copy_ms * 1e3, "gbs": 2 * half / (copy_ms * 1e-3) / 1e9},
+            "iters": iters}
+
+
+def run_packs(fp, groups, h, first, count, batch=None):
+    for i in range(first, first + count):
+        if batch is not None:
+            batch.pack(fp, h, i & 1)
+            continue
+        for grp in groups:
+            grp.sets[i & 1].pack(fp, grp.L, h)
+
+
 def run_steps(fp, groups, h, first, count, evs=None, batch=None, rs=False):
     for i in range(first, first + count):
         if batch is not None:
@@ -618,6 +686,87 @@ def run_steps(fp, groups, h, first, count, evs=None, batch=None, rs=False):
             continue
         for gi, grp in enumerate(groups):
             grp.sets[i & 1].step(fp, grp.L, h, None if evs is None else evs[i - first][gi], rs)
+
+
+def capture(torch, fn):
+    """A CUDA graph of fn(stream) on a side stream (two packs or two steps)."""
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        fn(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return graph
+
+
+def timed_passes(fp, torch, groups, batch, h, K, warmup, rs, graph, gpu_id):
+    """The timed region (K packs of every group, back to back) and, right
+    after it, K whole steps; clocks sampled over both.  Returns the two
+    device times (max over ranks) and the clock record."""
+    run_steps(fp, groups, h, 0, warmup, batch=batch, rs=rs)
+    run_packs(fp, groups, h, 0, warmup, batch=batch)
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
+    g_pack = g_step = None
+    if graph:
+        g_pack = capture(torch, lambda s: run_packs(fp, groups, s, 0, 2, batch=batch))
+        g_step = capture(torch, lambda s: run_steps(fp, groups, s, 0, 2, batch=batch, rs=rs))
+        for _ in range(max(1, warmup // 2)):
+            g_pack.replay()
+            g_step.replay()
+        torch.cuda.synchronize()
+        for grp in groups:
+            fp.fsdp_sync_status(grp.L)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    sampler = ClockSampler(gpu_id)
+    torch.cuda.synchronize()
+    barrier()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first sample before the load starts
+    ev[0].record()
+    if g_pack is not None:
+        for _ in range(K // 2):
+            g_pack.replay()
+    else:
+        run_packs(fp, groups, h, 0, K, batch=batch)
+    ev[1].record()
+    ev[2].record()
+    if g_step is not None:
+        for _ in range(K // 2):
+            g_step.replay()
+    else:
+        run_steps(fp, groups, h, 0, K, batch=batch, rs=rs)
+    ev[3].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
+    dev = torch.device("cuda")
+    return (max_over_ranks(ev[0].elapsed_time(ev[1]), device=dev),
+            max_over_ranks(ev[2].elapsed_time(ev[3]), device=dev), clocks)
+
+
+def evented_ops(fp, torch, groups, batch, h, K, OPS, rs):
+    """Per-operation device times: the same steps with a CUDA event around
+    every launch (events between launches serialise them)."""
+    n_launch = 1 if batch is not None else len(groups)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(n_launch)]
+           for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier()
+    run_steps(fp, groups, h, 0, K, evs, batch=batch, rs=rs)
+    torch.cuda.synchronize()
+    barrier()
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
+    return {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs] for j, k in enumerate(OPS)}
+
+
+def op_rows(nbytes, per, n_launch):
+    return {k: {"bytes": nbytes[k], "launches_per_step": n_launch, "ms_mean": statistics.mean(v),
+                "ms_median": statistics.median(v), "ms_min": min(v),
+                "gbs": nbytes[k] / (statistics.mean(v) * 1e-3) / 1e9}
+            for k, v in per.items()}
 
 
 def run_ours(args):
@@ -644,84 +793,45 @@ def run_ours(args):
     batch = Batch(fp, groups) if args.batched else None
     n_launch = 1 if batch is not None else len(groups)
     rs = args.rs_copy_out
-    run_steps(fp, groups, h, 0, args.warmup, batch=batch, rs=rs)
-    for grp in groups:
-        fp.fsdp_sync_status(grp.L)
-
-    K = args.steps
-    graph = None
-    if args.graph:
-        # Two steps (buffer sets 0 and 1) captured once and replayed K / 2
-        # times: the layers' launches go to the GPU without host involvement.
-        K += K & 1
-        graph = torch.cuda.CUDAGraph()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(graph):
-            run_steps(fp, groups, torch.cuda.current_stream().cuda_stream, 0, 2, batch=batch, rs=rs)
-        for _ in range(max(1, args.warmup // 2)):
-            graph.replay()
-        torch.cuda.synchronize()
-        for grp in groups:
-            fp.fsdp_sync_status(grp.L)
+    K = args.steps + (args.steps & 1 if args.graph else 0)
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:
         pass
-    # Pass 1: the timed region proper.  Launches follow each other with
-    # nothing in between, as in a training step.
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(gpu_id)
-    torch.cuda.synchronize()
-    barrier()
-    sampler.start()
-    time.sleep(0.3)  # let the sampler take its first sample before the load starts
-    t_start.record()
-    if graph is not None:
-        for _ in range(K // 2):
-            graph.replay()
-    else:
-        run_steps(fp, groups, h, 0, K, batch=batch, rs=rs)
-    t_end.record()
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    barrier()
-    for grp in groups:
-        fp.fsdp_sync_status(grp.L)
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), device=torch.device("cuda"))
+    pack_total_ms, step_total_ms, clocks = timed_passes(fp, torch, groups, batch, h, K, args.warmup, rs,
+                                                        args.graph, gpu_id)
+    per = evented_ops(fp, torch, groups, batch, h, min(K, args.evented_steps), OPS, rs)
 
-    # Pass 2: the same K steps with a CUDA event around every launch, for the
-    # per-operation device times (events between launches serialise them).
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(n_launch)]
-           for _ in range(K)]
-    torch.cuda.synchronize()
-    barrier()
-    run_steps(fp, groups, h, 0, K, evs, batch=batch, rs=rs)
-    torch.cuda.synchronize()
-    barrier()
-    for grp in groups:
-        fp.fsdp_sync_status(grp.L)
-    per = {k: [sum(e[j].elapsed_time(e[j + 1]) for e in step) for step in evs] for j, k in enumerate(OPS)}
-
+    refs = same_run_references(fp, torch, nbytes["pack"], args.reference_iters) if args.reference_iters > 0 else None
     precast = None
     if len(groups) == 1 and args.precast_iters > 0:
         precast = precast_comparison(fp, torch, work, groups[0], h, args.precast_iters, rows)
-
-    e2e = None
+    e2e = step_e2e = None
     if args.e2e_steps > 0:
-        e2e = run_e2e(args, fp, torch, groups, h, rs, step_bytes, world)
+        e2e = run_e2e(args, fp, torch, groups, h, rs, nbytes["pack"], world, whole_step=False)
+        step_e2e = run_e2e(args, fp, torch, groups, h, rs, step_bytes, world, whole_step=True)
+    extra = None
+    if args.extra and world == 1 and args.workload == "mixed50m":
+        extra = {}
+        for name, wname, batched in EXTRA_WORKLOADS:
+            extra[name] = run_extra(fp, torch, h, wname, batched, gpu_id)
+    elif args.extra:
+        extra = {"skipped": "only with the default workload at N = 1 (the extra workloads are per-GPU "
+                            "figures; replicas would repeat them)"}
 
     result = None
     if rank == 0:
-        result = report(args, work, description, groups, nbytes, step_bytes, total_ms, per, clocks, e2e,
-                        n_launch, rs, world, K)
+        result = report(args, work, description, groups, nbytes, step_bytes, pack_total_ms, step_total_ms, per,
+                        clocks, e2e, step_e2e, n_launch, world, K, refs)
         if precast is not None:
             result["precast_baseline"] = precast
+        if extra is not None:
+            result["extra_workloads"] = extra
     for grp in groups:
         grp.L.close()
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        samp = OracleSampler(work, inputs, rows)
-        result["cpu_baseline"] = cpu_baseline(samp, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(OracleSampler(work, inputs, rows), args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)
     import torch.distributed as dist
@@ -729,27 +839,70 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, fp, torch, groups, h, rs, step_bytes, world):
-    # End to end through the same API with host buffers: every step copies
-    # its inputs from pinned host memory and reads its results back.  Steps
-    # are pipelined the way a caller would run them: uploads on one stream,
-    # the kernels on another, downloads on a third, two buffer sets, so step
+# The extra workloads of the default run: (key, workload, batched).
+EXTRA_WORKLOADS = (("transformer500_batched", "transformer500", True), ("kda_block_w64", "kda_w64", False))
+
+
+def run_extra(fp, torch, h, wname, batched, gpu_id, seconds=0.5):
+    """One more workload, about `seconds` of packs and of whole steps each,
+    with inputs drawn on the device: pack, copy-in and copy-out times and the
+    pack's fraction of the measured copy bandwidth, with its own clocks."""
+    factory, description = WORKLOADS[wname]
+    work = factory()
+    groups = [Group(fp, torch, work, g, device_inputs(work, g)) for g in range(len(work.groups))]
+    batch = Batch(fp, groups) if batched else None
+    n_launch = 1 if batch is not None else len(groups)
+    OPS = ("pack", "copy_in", "copy_out")
+    nbytes = {k: sum(grp.nbytes[k] for grp in groups) for k in OPS}
+    step_bytes = sum(nbytes.values())
+    probe_ms = loop_ms(torch, lambda k: run_packs(fp, groups, h, k, 1, batch=batch), 20)
+    K = max(20, int(seconds / (probe_ms * 1e-3)))
+    K += K & 1
+    pack_ms, step_ms, clocks = timed_passes(fp, torch, groups, batch, h, K, 10, False, False, gpu_id)
+    per = evented_ops(fp, torch, groups, batch, h, min(K, 500), OPS, False)
+    peak, peak_kind = read_peaks()
+    pack_gbs = nbytes["pack"] * K / (pack_ms * 1e-3) / 1e9
+    out = {"workload": description, "groups": len(groups), "launches_per_op": n_launch, "steps": K,
+           "pack": {"bytes": nbytes["pack"], "us": pack_ms * 1e3 / K, "gbs": pack_gbs, "frac": pack_gbs / peak,
+                    "frac_of_nominal_8tbs": pack_gbs / NOMINAL_HBM_GBS, "peak": peak, "peak_source": peak_kind},
+           "hot_path_step": {"bytes": step_bytes, "us": step_ms * 1e3 / K,
+                             "gbs": step_bytes * K / (step_ms * 1e-3) / 1e9},
+           "ops": op_rows(nbytes, per, n_launch), "clocks": clocks}
+    for grp in groups:
+        grp.L.close()
+    del groups, batch
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_e2e(args, fp, torch, groups, h, rs, nbytes, world, whole_step):
+    # End to end through the same API with host buffers.  Pack only: every
+    # step uploads the gradients from pinned host memory and downloads the
+    # packed buckets.  Whole step: also the shards and the other ranks' rows
+    # up, the full parameters (and sharded gradients) down.  Steps are
+    # pipelined the way a caller would run them: uploads on one stream, the
+    # kernels on another, downloads on a third, two buffer sets, so step
     # i+1's uploads overlap step i's downloads.
     pin = lambda n: torch.empty(n, dtype=torch.uint8, pin_memory=True)  # noqa: E731
     host = []
     for grp in groups:
         s0 = grp.sets[0]
-        hb = {"grads": pin(s0.grads.numel()), "shards": pin(s0.shards.numel()),
-              "others": pin(s0.gathered.numel() - s0.S_ag),
-              "out": [{"buckets": [pin(b.numel()) for b in s0.buckets], "full": pin(s0.full.numel()),
-                       "sharded": pin(s0.sharded.numel()) if rs else None} for _ in range(2)]}
+        hb = {"grads": pin(s0.grads.numel()),
+              "out": [{"buckets": [pin(b.numel()) for b in s0.buckets]} for _ in range(2)]}
         hb["grads"].copy_(s0.grads.cpu())
-        hb["shards"].copy_(s0.shards.cpu())
-        hb["others"].copy_(s0.gathered[s0.S_ag:].cpu())
+        if whole_step:
+            hb["shards"], hb["others"] = pin(s0.shards.numel()), pin(s0.gathered.numel() - s0.S_ag)
+            hb["shards"].copy_(s0.shards.cpu())
+            hb["others"].copy_(s0.gathered[s0.S_ag:].cpu())
+            for o in hb["out"]:
+                o["full"] = pin(s0.full.numel())
+                o["sharded"] = pin(s0.sharded.numel()) if rs else None
         host.append(hb)
-    h2d = sum(hb["grads"].numel() + hb["shards"].numel() + hb["others"].numel() for hb in host)
-    d2h = sum(sum(b.numel() for b in hb["out"][0]["buckets"]) + hb["out"][0]["full"].numel()
-              + (hb["out"][0]["sharded"].numel() if rs else 0) for hb in host)
+    h2d = sum(hb["grads"].numel() + (hb["shards"].numel() + hb["others"].numel() if whole_step else 0)
+              for hb in host)
+    d2h = sum(sum(b.numel() for b in hb["out"][0]["buckets"])
+              + (hb["out"][0]["full"].numel() + (hb["out"][0]["sharded"].numel() if rs else 0) if whole_step else 0)
+              for hb in host)
     E = max(3, args.e2e_steps)
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     main = torch.cuda.current_stream()
@@ -768,12 +921,16 @@ def run_e2e(args, fp, torch, groups, h, rs, step_bytes, world):
                 for grp, hb in zip(groups, host):
                     sk = grp.sets[k]
                     sk.grads.copy_(hb["grads"], non_blocking=True)
-                    sk.shards.copy_(hb["shards"], non_blocking=True)
-                    sk.gathered[sk.S_ag:].copy_(hb["others"], non_blocking=True)
+                    if whole_step:
+                        sk.shards.copy_(hb["shards"], non_blocking=True)
+                        sk.gathered[sk.S_ag:].copy_(hb["others"], non_blocking=True)
                 uploaded[k].record(up)
             main.wait_event(uploaded[k])
             for grp in groups:
-                grp.sets[k].step(fp, grp.L, h, None, rs)
+                if whole_step:
+                    grp.sets[k].step(fp, grp.L, h, None, rs)
+                else:
+                    grp.sets[k].pack(fp, grp.L, h)
             computed[k].record(main)
             with torch.cuda.stream(down):
                 down.wait_event(computed[k])
@@ -781,9 +938,10 @@ def run_e2e(args, fp, torch, groups, h, rs, step_bytes, world):
                     sk, ho = grp.sets[k], hb["out"][k]
                     for hbuf, dbuf in zip(ho["buckets"], sk.buckets):
                         hbuf.copy_(dbuf, non_blocking=True)
-                    ho["full"].copy_(sk.full, non_blocking=True)
-                    if rs:
-                        ho["sharded"].copy_(sk.sharded, non_blocking=True)
+                    if whole_step:
+                        ho["full"].copy_(sk.full, non_blocking=True)
+                        if rs:
+                            ho["sharded"].copy_(sk.sharded, non_blocking=True)
                 downloaded[k].record(down)
         main.wait_stream(up)
         main.wait_stream(down)
@@ -800,62 +958,76 @@ def run_e2e(args, fp, torch, groups, h, rs, step_bytes, world):
     for grp in groups:
         fp.fsdp_sync_status(grp.L)
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device=torch.device("cuda"))
-    return {"value": world * step_bytes * E / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
-            "note": "host buffers; uploads, kernels and downloads of consecutive steps pipelined "
+    what = ("whole step (pack, copy-in, copy-out" + (", rs copy-out" if rs else "") + ")") if whole_step else \
+        "the reduce-scatter pack"
+    return {"value": world * nbytes * E / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": e2e_ms / E,
+            "note": f"{what} with host buffers; uploads, kernels and downloads of consecutive steps pipelined "
                     "on three streams with two buffer sets"}
 
 
-def report(args, work, description, groups, nbytes, step_bytes, total_ms, per, clocks, e2e, n_launch, rs,
-           world, K):
+def report(args, work, description, groups, nbytes, step_bytes, pack_total_ms, step_total_ms, per, clocks, e2e,
+           step_e2e, n_launch, world, K, refs):
     """The JSON result of our arm (rank 0)."""
     peak, peak_kind = read_peaks()
-    pack_ms = statistics.mean(per["pack"])
-    achieved = nbytes["pack"] / (pack_ms * 1e-3) / 1e9
-    rows = {k: {"bytes": nbytes[k], "launches_per_step": n_launch, "ms_mean": statistics.mean(v),
-                "ms_median": statistics.median(v), "ms_min": min(v),
-                "gbs": nbytes[k] / (statistics.mean(v) * 1e-3) / 1e9}
-            for k, v in per.items()}
+    pack_ms = pack_total_ms / K
+    achieved = nbytes["pack"] / (pack_ms * 1e-3) / 1e9   # per GPU
+    roofline = {"bound": "hbm", "kernel": "walk_kernel (the reduce-scatter pack launches)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "peak_source": f"{peak_kind} hbm_gbs (burst copy)" if peak_kind == "measured" else "fallback",
+                "bytes_per_launch": nbytes["pack"] / n_launch,
+                "timing": "mean per pack over the timed region (K packs back to back, CUDA events around the "
+                          "whole region on the launching stream)",
+                "traffic": None}
+    if args.workload == "mixed50m" and not args.row_chunks and n_launch == 1:
+        t = read_traffic()
+        if t is not None:
+            roofline.update(t)
+            roofline["traffic_note"] = ("DRAM bytes of one cold ncu capture of the pack; "
+                                        "traffic_l2_write counts L2 write sectors x 32 B")
+    if refs is not None:
+        for r in (refs["plain_widen_1to2"], refs["copy_1to1"]):
+            r["pack_over_this"] = achieved / r["gbs"]
+        roofline["same_run_references"] = refs
     result = {
         "metric": METRIC,
-        "value": world * step_bytes * K / (total_ms * 1e-3) / 1e9,
+        "value": world * nbytes["pack"] * K / (pack_total_ms * 1e-3) / 1e9,
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": total_ms / K,
+        "ms_per_step": pack_ms,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16+f32",
         "data": "synthetic",
-        "config": {"workload": f"{description}; {STEP}" + (STEP_RS if rs else "")
-                   + (STEP_ERS if args.emulated_rs else ""), "world_size_layout": work.W,
-                   "chunking": CHUNKING[args.row_chunks],
-                   "groups": len(groups), "launches_per_op": n_launch, "step_bytes": step_bytes,
-                   "launch": ("CUDA graph of two steps, replayed" if args.graph
-                              else "stream launches from the host") + (", batched over groups" if args.batched else ""),
-                   "parallelism": f"replicas x{world} (no data-path collective)",
-                   "l2": "inputs larger than L2: two rotating buffer sets of "
-                         f"{2 * step_bytes / 1e9:.2f} GB of algorithmic traffic vs 129 MB L2; no flush"},
-        "ops": rows,
-        "ops_note": "per-operation device times from a second pass of the same K steps with CUDA "
-                    "events around every launch (summed over the step's groups)",
-        "roofline": {"bound": "hbm", "kernel": "walk_kernel (reduce-scatter pack launches)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)" if peak_kind == "measured" else "fallback",
-                     "bytes_per_launch": nbytes["pack"] / n_launch,
-                     "traffic": read_traffic() if args.workload == "mixed50m" else None},
+        "config": make_config(args, work, description, len(groups), n_launch, nbytes["pack"], world),
+        "step_note": "one step = the reduce-scatter pack of every group of the workload (the operation the "
+                     "metric names); ms_per_step is the pack's ms per fully_shard group" +
+                     (" (all groups)" if len(groups) > 1 else ""),
+        "hot_path_step": {"what": STEP + (STEP_RS if args.rs_copy_out else "")
+                          + (STEP_ERS if args.emulated_rs else ""),
+                          "bytes": step_bytes, "steps": K, "ms_per_step": step_total_ms / K,
+                          "gbs": world * step_bytes * K / (step_total_ms * 1e-3) / 1e9,
+                          "timing": "K whole steps back to back right after the timed region, same clocks"},
+        "ops": op_rows(nbytes, per, n_launch),
+        "ops_note": "per-operation device times from a pass of whole steps with CUDA events around every "
+                    "launch (summed over the step's groups)",
+        "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": len(per) * n_launch * K,
+        "hot_path_step_e2e": step_e2e,
+        "gpu_launches": K * n_launch,
+        "gpu_launches_note": "walk_kernel launches inside the timed region (the packs); the whole-step pass "
+                             "after it launches 3 per group and step",
         "clocks": clocks,
     }
     return result
 
 
 # ---------------------------------------------------------------------------
-# Reference arm: the CPU oracle, each step one bounded segment of the step.
+# Reference arm: the CPU oracle's pack, each step one bounded run of it.
 # ---------------------------------------------------------------------------
 def run_reference(args):
     rank, world, _ = dist_env()
@@ -873,17 +1045,18 @@ def run_reference(args):
         done += samp.next()
     dt = time.perf_counter() - t0
     value = done / dt / 1e9
+    n_launch = 1 if args.batched else len(work.groups)
     result = {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32", "data": "synthetic",
-        "config": {"workload": f"{description}; {STEP}", "world_size_layout": work.W,
-                   "chunking": CHUNKING[args.row_chunks],
-                   "groups": len(work.groups), "step_bytes": samp.step_bytes, "parallelism": "single host thread"},
+        "config": make_config(args, work, description, len(work.groups), n_launch, samp.pack_bytes, world),
+        "step_note": "one step = one (bucket, rank, parameter) run of the reduce-scatter pack on the CPU oracle, "
+                     f"cycling through the {len(samp.segs)} runs of the workload's pack; value = bytes / time",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "each step = one (rank, parameter) run of the pack, copy-in or copy-out, "
-                                   f"cycling through the {len(samp.segs)} runs of a whole step", **host_cpu()},
+                         "sample": f"{args.steps} runs of the reduce-scatter pack "
+                                   f"({done / samp.pack_bytes:.2f} whole packs)", **host_cpu()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(result), flush=True)

@@ -14,10 +14,12 @@
 // The work is bound by HBM bandwidth, so the kernel is a warp-specialised
 // pipeline built to keep many bytes in flight per SM with few registers and
 // to write only full, aligned 16-byte vectors:
-//   * warp 0, lane 0 is the producer.  For each item of its CTA it copies the
-//     item's source bytes, widened to whole aligned 16-byte blocks, into one
-//     stage of a shared-memory ring with one TMA bulk copy (cp.async.bulk),
-//     completion counted on that stage's "full" mbarrier;
+//   * warp 0 first resolves the CTA's first items (descriptor and source /
+//     destination pointers) in parallel, one per lane; then lane 0 is the
+//     producer.  For each item of its CTA it copies the item's source bytes,
+//     widened to whole aligned 16-byte blocks, into one stage of a
+//     shared-memory ring with one TMA bulk copy (cp.async.bulk), completion
+//     counted on that stage's "full" mbarrier;
 //   * warps 1..8 are consumers.  For each item they wait on the stage, then
 //     write the destination as 16-byte vectors: each lane reads the source
 //     bytes of one vector from shared memory at whatever byte phase they have
@@ -66,7 +68,16 @@ constexpr int kStageDataBytes = (int)kStageBytes + 32;
 constexpr int kHeaderBytes = 64;
 constexpr int kStageStride = (kStageDataBytes + kHeaderBytes + 127) / 128 * 128;
 static_assert(kStageDataBytes % 16 == 0, "stage header must stay 16-byte aligned");
-constexpr int kSmemBytes = kStages * kStageStride + 2 * kStages * 8;
+// After the stages and their barriers: the resolved headers of a CTA's first
+// kPrefetch items (StageHeader, 32 bytes each), then, for batched launches,
+// the layouts' first global item indices (kMaxBatch + 1 int64).
+constexpr int kPrefetch = 32;
+constexpr int kMaxBatch = 64;
+constexpr int kBarrierBytes = 2 * kStages * 8;
+constexpr int kPrefetchOffset = kStages * kStageStride + kBarrierBytes;
+constexpr int kStartOffset = kPrefetchOffset + kPrefetch * 32;
+constexpr int kSmemBytes = kStartOffset + (kMaxBatch + 1) * 8;
+static_assert(kPrefetchOffset % 16 == 0 && kStartOffset % 16 == 0, "shared tables must stay 16-byte aligned");
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 // Status bits written by a kernel whose bounded wait gave up.
@@ -97,7 +108,8 @@ constexpr int32_t kSchedMixed = 1;
 // Per-call pointers travel by value in the parameter block: `slot` is read
 // with a run-time index, which __grid_constant__ allows without a local copy.
 // fetch(i) returns work item i and the slot base its slot numbers are
-// relative to; `cursor` carries the layout of the CTA's previous item.
+// relative to; `cursor` carries the layout of the CTA's previous item and
+// `tab` is the launch's table in shared memory (see prepare).
 template <int NSLOT>
 struct LaunchArgs {
   const WorkItem *items;
@@ -109,7 +121,13 @@ struct LaunchArgs {
   Sched sched;
   const void *slot[NSLOT];
 
-  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *) const {
+  // Nothing to copy into shared memory for a single layout.
+  __device__ __forceinline__ void prepare(int64_t *, int) const {}
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *, const int64_t *) const {
+    *base = 0;
+    return items[i];
+  }
+  __device__ __forceinline__ WorkItem fetch_any(int64_t i, int32_t *base, const int64_t *) const {
     *base = 0;
     return items[i];
   }
@@ -117,7 +135,6 @@ struct LaunchArgs {
 
 // Several layouts in one launch: the items of layout g are global items
 // [start[g], start[g+1]); their slots are numbered from slot_base[g].
-constexpr int kMaxBatch = 64;
 template <int NSLOT>
 struct BatchArgs {
   int64_t n_items;
@@ -131,18 +148,39 @@ struct BatchArgs {
   int32_t slot_base[kMaxBatch];
   const void *slot[NSLOT];
 
-  // The last group that starts at or before i, found by walking forward
-  // from the CTA's previous one: a CTA's item indices grow (except after the
-  // rare retake of the work-sharing word, which restarts the walk), so the
-  // walk costs about one step per layout instead of a chain of dependent
-  // parameter loads per item.
-  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *cursor) const {
-    int g = *cursor;
-    if (start[g] > i) g = 0;
-    while (g + 1 < n_groups && start[g + 1] <= i) ++g;
-    *cursor = g;
+  // Warp 0 copies start[0 .. n_groups] into shared memory (`tab`), where the
+  // producer's lookups read it instead of the parameter block.
+  __device__ __forceinline__ void prepare(int64_t *tab, int lane) const {
+    for (int g = lane; g <= n_groups; g += 32) tab[g] = start[g];
+  }
+  __device__ __forceinline__ WorkItem at(int g, int64_t i, int32_t *base, const int64_t *tab) const {
     *base = slot_base[g];
-    return items[g][i - start[g]];
+    return items[g][i - tab[g]];
+  }
+  // The last group that starts at or before i, found by walking forward
+  // from the CTA's previous one (`cursor`; -1 or a group past i: bisection
+  // first): a CTA's item indices grow, so the walk costs about one step per
+  // layout over the launch.
+  // The group of item i by bisection: the last group that starts at or
+  // before i (every group of the launch holds at least one item).
+  __device__ __forceinline__ int locate(int64_t i, const int64_t *tab) const {
+    int lo = 0, hi = n_groups - 1;  // tab[lo] <= i, and the answer is at most hi
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tab[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  }
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *cursor, const int64_t *tab) const {
+    int g = *cursor;
+    if (g < 0 || tab[g] > i) g = locate(i, tab);
+    while (g + 1 < n_groups && tab[g + 1] <= i) ++g;
+    *cursor = g;
+    return at(g, i, base, tab);
+  }
+  __device__ __forceinline__ WorkItem fetch_any(int64_t i, int32_t *base, const int64_t *tab) const {
+    return at(locate(i, tab), i, base, tab);
   }
 };
 
@@ -201,8 +239,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 // Programmatic dependent launch.  Every launch allows the next kernel on the
 // stream to be scheduled early (launch_dependents), and waits for the
 // previous kernel on the stream to finish and publish its memory
-// (griddepcontrol.wait) before touching any input or output.  Only the
-// immutable work table is read before the wait.
+// (griddepcontrol.wait) before touching any input or output.  Only the work
+// table and the parameter block are read before the wait: a layout's table
+// never changes after planning, and the allocation-free pack, whose table is
+// rewritten before each of its launches, launches without programmatic
+// serialization (see noalloc_launch).
 __device__ __forceinline__ void wait_for_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -313,6 +354,7 @@ struct StageHeader {
   int32_t reserved;
 };
 static_assert(sizeof(StageHeader) <= kHeaderBytes, "stage header too large");
+static_assert(sizeof(StageHeader) == 32, "the prefetch table holds 32-byte headers");
 constexpr int32_t kSkipItem = -1;
 constexpr int32_t kDoneItem = -2;  // no item follows: the consumers leave
 
@@ -461,11 +503,29 @@ __device__ __forceinline__ void consume_item(const char *src, char *dst, int n_c
   }
 }
 
+// The header of work item w as the consumers read it: its source and
+// destination pointers resolved from the launch's slots (`base` is the slot
+// base of its layout).  Reads only the parameter block.
+template <class Args>
+__device__ __forceinline__ StageHeader resolve_item(const Args &a, const WorkItem &w, int32_t base) {
+  const int ss = (w.kind & 1) ? 2 : 4, ds = (w.kind & 2) ? 2 : 4;
+  StageHeader h;
+  h.src = reinterpret_cast<const char *>(a.slot[base + w.src_slot]) + w.src_off * (int64_t)ss;
+  h.dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[base + w.dst_slot])) + w.dst_off * (int64_t)ds;
+  h.n_copy = w.n_copy;
+  h.n_total = w.n_total;
+  h.kind = w.kind;
+  h.reserved = 0;
+  return h;
+}
+
 template <class Args>
 __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageStride);
   uint64_t *empty = full + kStages;
+  StageHeader *pre = reinterpret_cast<StageHeader *>(smem + kPrefetchOffset);
+  int64_t *tab = reinterpret_cast<int64_t *>(smem + kStartOffset);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -478,40 +538,64 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
 
   const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
   if (warp == 0) {
-    if (lane != 0) return;
-    // Producer.  Item indices are claimed two items ahead of use and their
-    // descriptors fetched one ahead, so neither the work-sharing word's
-    // round trip nor the descriptor load sits on a stage hand-off: issue()
-    // starts a claim without looking at what a shared claim's atomic add
-    // returns, and resolve() turns it into an index one item later.
     const int64_t G = gridDim.x, n = a.n_items;
     const Sched sc = a.sched;
     const int64_t shared0 = sc.word ? sc.fixed_rounds * G : 0;  // first shared item
+    // This CTA's fixed-order items are blockIdx.x + m * G below fixed_end
+    // (at least one: the grid is at most n, and a launch that shares items
+    // keeps at least one fixed round).  Before waiting for the previous
+    // kernel, the warp's lanes resolve the first kPrefetch of them at once --
+    // descriptor from the work table, source and destination pointers from
+    // the parameter block -- into `pre`.  Done by one thread, each item's
+    // lookups are a chain of dependent loads that miss the caches on a fresh
+    // launch, and that chain would sit between consecutive bulk copies.
+    const int64_t fixed_end = sc.word ? (shared0 < n ? shared0 : n) : n;
+    const int64_t n_fixed = (int64_t)blockIdx.x < fixed_end ? (fixed_end - blockIdx.x + G - 1) / G : 0;
+    const int n_pre = (int)(n_fixed < kPrefetch ? n_fixed : kPrefetch);
+    a.prepare(tab, lane);
+    __syncwarp();
+    if (lane < n_pre) {
+      int32_t base = 0;
+      const WorkItem w = a.fetch_any(blockIdx.x + (int64_t)lane * G, &base, tab);
+      pre[lane] = resolve_item(a, w, base);
+    }
+    __syncwarp();
+    if (lane != 0) return;
+    // Producer (lane 0).  Item indices are claimed two items ahead of use,
+    // and the descriptors of items past the prefetched ones are fetched one
+    // ahead, so neither the work-sharing word's round trip nor a descriptor
+    // load sits on a stage hand-off: issue() starts a claim without looking
+    // at what a shared claim's atomic add returns, and take() turns it into
+    // an index one item later.
     // part 0: fixed-order items; 1: user of the word; 2: fixed order over
     // [shared0, n); 3: nothing left.
     int part = sc.word ? 0 : 2;
     int64_t m = 0;
     struct Claim {
       unsigned long long v;  // an item index, or the word's value before a shared claim's add
+      int32_t pm;            // >= 0: the item's resolved header is pre[pm]
       bool shared;
     };
     auto issue = [&]() -> Claim {
       if (part == 0) {
-        if (m < sc.fixed_rounds) return Claim{(unsigned long long)(blockIdx.x + (m++) * G), false};
+        if (m < sc.fixed_rounds) {
+          const int64_t mm = m++;
+          return Claim{(unsigned long long)(blockIdx.x + mm * G), mm < n_pre ? (int32_t)mm : -1, false};
+        }
         m = 0;
         const bool mixed_out = (sc.flags & kSchedMixed) && (blockIdx.x & 1u);
         part = !mixed_out && sched_join(sc.word, sc.tag) ? 1 : 2;
       }
-      if (part == 1) return Claim{atomicAdd(sc.word, 1ull), true};
-      if (part == 2) return Claim{(unsigned long long)(shared0 + blockIdx.x + (m++) * G), false};
-      return Claim{(unsigned long long)n, false};
+      if (part == 1) return Claim{atomicAdd(sc.word, 1ull), -1, true};
+      if (part == 2) return Claim{(unsigned long long)(shared0 + blockIdx.x + (m++) * G), -1, false};
+      return Claim{(unsigned long long)n, -1, false};
     };
     // Claims resolve in the order they were issued.  Shared counts only grow
     // while this CTA is a user, so after the first shared claim past the end
     // every later one is past it too; the CTA leaves on the first.  Its adds
     // issued before the leave come first in the word's order (one thread,
     // one address), so the leave never lands ahead of them.
-    auto resolve = [&](Claim q) -> int64_t {
+    auto take = [&](Claim q) -> int64_t {
       if (!q.shared) return (int64_t)q.v;
       const int64_t i = shared0 + (int64_t)(q.v & kSchedCountMask);
       if (i < n) return i;
@@ -523,10 +607,10 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     };
     int64_t k = 0;
     bool skipped_first = false, stopped = false;
-    int cursor = 0;  // layout of the last fetched item (batched launches)
-    // Stage item w (slot base `base`) in the ring; false if the stage never
-    // came free (the wait gave up).
-    auto stage_item = [&](const WorkItem &w, int32_t base) -> bool {
+    int cursor = -1;  // layout of the last fetched item (batched launches; -1: none yet)
+    // Stage the item with resolved header h in the ring; false if the stage
+    // never came free (the wait gave up).
+    auto stage_item = [&](const StageHeader &h) -> bool {
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, a.wait_limit_ns)) {
@@ -538,53 +622,45 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         ++k;
         return true;
       }
-      const int ss = (w.kind & 1) ? 2 : 4, ds = (w.kind & 2) ? 2 : 4;
-      const char *src = reinterpret_cast<const char *>(a.slot[base + w.src_slot]) + w.src_off * (int64_t)ss;
-      const Staged st = staged_of(src, w.n_copy * ss);
+      const int ss = (h.kind & 1) ? 2 : 4;
+      const Staged st = staged_of(h.src, h.n_copy * ss);
       uint32_t bytes = (uint32_t)st.bytes;
       StageHeader *hd = reinterpret_cast<StageHeader *>(smem + s * kStageStride + kStageDataBytes);
-      hd->src = src;
-      hd->dst = reinterpret_cast<char *>(const_cast<void *>(a.slot[base + w.dst_slot])) + w.dst_off * (int64_t)ds;
-      hd->n_copy = w.n_copy;
-      hd->n_total = w.n_total;
-      hd->kind = w.kind;
+      *hd = h;
       if (bytes > (uint32_t)kStagedMax) {  // never planned; the consumers skip it
         atomicOr(a.status, kStatusBadItem);
         hd->kind = kSkipItem;
         bytes = 0;
       }
       mbar_arrive_expect_tx(&full[s], bytes);
-      if (bytes) bulk_copy_g2s(smem + s * kStageStride, src - st.lead, bytes, &full[s]);
+      if (bytes) bulk_copy_g2s(smem + s * kStageStride, h.src - st.lead, bytes, &full[s]);
       ++k;
       return true;
     };
-    // A CTA's first item is blockIdx.x in every schedule (a launch that
-    // shares items keeps at least one fixed round), so its descriptor is
-    // fetched before waiting for the previous kernel on the stream.
-    int32_t cur_base = 0;
-    WorkItem cur = a.fetch(blockIdx.x, &cur_base, &cursor);  // the grid is at most n
     wait_for_previous_grid();
     if (!sc.word) {
-      // Fixed order: items blockIdx.x + m * G, each descriptor fetched one
-      // item ahead.
-      for (int64_t i = blockIdx.x; i < n; i += G) {
-        const WorkItem w = cur;
-        const int32_t base = cur_base;
-        if (i + G < n) cur = a.fetch(i + G, &cur_base, &cursor);
-        if (!stage_item(w, base)) {
+      // Fixed order: items blockIdx.x + mi * G; past the prefetched ones,
+      // each descriptor is fetched one item ahead.
+      WorkItem nxt{};
+      int32_t nxt_base = 0;
+      for (int64_t i = blockIdx.x, mi = 0; i < n; i += G, ++mi) {
+        const StageHeader h = mi < n_pre ? pre[mi] : resolve_item(a, nxt, nxt_base);
+        if (mi + 1 >= n_pre && i + G < n) nxt = a.fetch(i + G, &nxt_base, &cursor, tab);
+        if (!stage_item(h)) {
           stopped = true;
           break;
         }
       }
     } else {
-      // Shared: each round issues the claim two items ahead and resolves the
-      // one issued the round before (a first round only primes that queue),
-      // so neither the word's round trip nor the descriptor load sits on a
-      // stage hand-off.  Joining the word comes after the wait above, when
-      // an earlier launch of the same operation on the stream has let go of
-      // it.
+      // Shared: each round issues the claim two items ahead and takes the
+      // one issued the round before (a first round only primes that queue).
+      // Item c0 is in hand: prefetched (c0_pm >= 0) or its descriptor
+      // fetched.  Joining the word comes after the wait above, when an
+      // earlier launch of the same operation on the stream has let go of it.
       m = 1;
       int64_t c0 = blockIdx.x;
+      int32_t c0_pm = 0, c0_base = 0;
+      WorkItem c0_w{};
       Claim q1{};
       bool primed = false;
       while (c0 < n) {
@@ -594,13 +670,15 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
           primed = true;
           continue;
         }
-        const WorkItem w = cur;
-        const int32_t base = cur_base;
-        const int64_t c1 = resolve(q1);
-        if (c1 < n) cur = a.fetch(c1, &cur_base, &cursor);
+        const StageHeader h = c0_pm >= 0 ? pre[c0_pm] : resolve_item(a, c0_w, c0_base);
+        const int64_t c1 = take(q1);
+        if (c1 < n) {
+          c0_pm = q1.pm;
+          if (c0_pm < 0) c0_w = a.fetch(c1, &c0_base, &cursor, tab);
+        }
         q1 = qn;
         c0 = c1;
-        if (!stage_item(w, base)) {
+        if (!stage_item(h)) {
           stopped = true;
           break;
         }
@@ -911,6 +989,26 @@ __global__ void __launch_bounds__(kSumThreads) sum_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
+// Plain streaming widen (a measurement utility): dst[i] = bits(src[i]) << 16,
+// BF16 to FP32, the pack's own 1 : 2 mix of bytes read to bytes written.
+// Grid-stride over 16-byte vectors of the source; each thread loads one
+// vector (streaming, read once) and stores the two 16-byte vectors it
+// widens to, so every warp store covers 1 KiB of contiguous destination.
+// ---------------------------------------------------------------------------
+constexpr int kWidenThreads = 256;
+constexpr int kWidenBlocksPerSm = 32;
+
+__global__ void __launch_bounds__(kWidenThreads) widen_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                              int64_t nvec) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    const uint4 x = __ldcs(src + v);
+    dst[2 * v] = make_uint4(x.x << 16, x.x & 0xFFFF0000u, x.y << 16, x.y & 0xFFFF0000u);
+    dst[2 * v + 1] = make_uint4(x.z << 16, x.z & 0xFFFF0000u, x.w << 16, x.w & 0xFFFF0000u);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host-side argument checks (nothing is launched unless all pass).
 // ---------------------------------------------------------------------------
 fsdp_status_t check_layout(const fsdp_layout *L) {
@@ -1006,16 +1104,17 @@ fsdp_status_t noalloc_launch(const WorkItem *items, int64_t n_items, uint32_t *s
   a.sched = Sched{nullptr, 0, 0, 0};  // fixed order: the array holds no work-sharing word
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // No programmatic stream serialization here: the kernel reads its work
+  // table before griddepcontrol.wait, and this table was just rewritten on
+  // the stream.  With plain stream order the launch starts only after
+  // everything before it on the stream, whatever that is, has finished.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   void *args[] = {&a};
   cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&walk_kernel<LaunchArgs<NSLOT>>), args);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
@@ -1414,6 +1513,34 @@ fsdp_status_t fsdp_pack_reduce_scatter_noalloc(const fsdp_layout_t *L, const voi
   if (P + B <= kSlotsSmall) return noalloc_launch<kSlotsSmall>(table, count, status, grid, ptrs, P + B, s);
   if (P + B <= kSlotsMedium) return noalloc_launch<kSlotsMedium>(table, count, status, grid, ptrs, P + B, s);
   return noalloc_launch<kSlotsLarge>(table, count, status, grid, ptrs, P + B, s);
+}
+
+fsdp_status_t fsdp_debug_stream_widen(const void *src, int64_t n, void *dst, fsdp_stream_t stream) {
+  if (n < 0 || n % 8 != 0) return fail(FSDP_EINVAL, "n must be a non-negative multiple of 8");
+  if (n == 0) {
+    clear_error();
+    return FSDP_OK;
+  }
+  if (!src || !dst) return fail(FSDP_EINVAL, "src or dst is NULL");
+  if (((uintptr_t)src | (uintptr_t)dst) & 15u) return fail(FSDP_EINVAL, "src and dst must be 16-byte aligned");
+  const uintptr_t s0 = (uintptr_t)src, s1 = s0 + (uintptr_t)n * 2, d0 = (uintptr_t)dst, d1 = d0 + (uintptr_t)n * 4;
+  if (s0 < d1 && d0 < s1) return fail(FSDP_EINVAL, "src and dst overlap");
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("device query failed: ") + cudaGetErrorString(e));
+  const int64_t nvec = n / 8;
+  int64_t grid = (int64_t)(sms > 0 ? sms : 1) * kWidenBlocksPerSm;
+  const int64_t need = (nvec + kWidenThreads - 1) / kWidenThreads;
+  if (grid > need) grid = need;
+  const uint4 *s = static_cast<const uint4 *>(src);
+  uint4 *d = static_cast<uint4 *>(dst);
+  void *args[] = {&s, &d, const_cast<int64_t *>(&nvec)};
+  e = cudaLaunchKernel(reinterpret_cast<const void *>(&widen_kernel), dim3((unsigned)grid), dim3(kWidenThreads), args, 0,
+                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  clear_error();
+  return FSDP_OK;
 }
 
 void fsdp_debug_set_upload_fault(int32_t fail_upload) {

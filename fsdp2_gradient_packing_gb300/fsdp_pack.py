@@ -100,6 +100,7 @@ _SIGNATURES = {
     "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
     "fsdp_debug_set_upload_fault": (None, [ctypes.c_int32]),
     "fsdp_debug_set_schedule": (_ST, [ctypes.c_int32]),
+    "fsdp_debug_stream_widen": (_ST, [_P, ctypes.c_int64, _P, _P]),
     "fsdp_layout_destroy": (None, [_LAYOUT]),
     "fsdp_status_string": (ctypes.c_char_p, [_ST]),
     "fsdp_last_error": (ctypes.c_char_p, []),
@@ -537,6 +538,12 @@ def fsdp_debug_set_upload_fault(fail_upload: bool) -> None:
 
 def fsdp_debug_set_schedule(mode: int) -> None:
     _check(_lib.fsdp_debug_set_schedule(mode), "fsdp_debug_set_schedule")
+
+
+def fsdp_debug_stream_widen(src, n: int, dst, stream=None) -> None:
+    """Plain BF16 -> FP32 streaming widen of n elements (a measurement
+    utility: the pack's 1 : 2 byte mix without its layout)."""
+    _check(_lib.fsdp_debug_stream_widen(_ptr(src), n, _ptr(dst), _stream(stream)), "fsdp_debug_stream_widen")
 
 
 def fsdp_layout_destroy(layout: Layout) -> None:

@@ -200,6 +200,25 @@ def device_random_bytes(nbytes: int, seed: int, *key: int):
     return torch.randint(0, 256, (int(nbytes),), dtype=torch.uint8, device="cuda", generator=g)
 
 
+def device_normal_bits(n: int, dtype: str, std: float, seed: int, *key: int):
+    """n seeded N(0, std) values as raw bits of ``dtype`` on the current CUDA
+    device (a uint8 tensor of n * element-size bytes), drawn by torch's
+    Philox generator.  BF16 values are the upper halves of FP32 draws, as in
+    normal_bits.  For timing inputs too large to draw on the host quickly;
+    the values differ from normal_bits' (another generator), the
+    distribution does not."""
+    import torch
+    state = np.random.SeedSequence([seed, *key]).generate_state(1, np.uint64)[0]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(int(state))
+    x = torch.randn(int(n), dtype=torch.float32, device="cuda", generator=g)
+    if std != 1.0:
+        x *= std
+    if dtype == "f32":
+        return x.view(torch.uint8)
+    return (x.view(torch.int32) >> 16).to(torch.int16).view(torch.uint8)
+
+
 # Special FP32 bit patterns: signed zeros, infinities, NaNs with payloads,
 # subnormals, extremes, and values whose low 16 bits sit exactly on, just
 # below and just above a BF16 rounding tie.

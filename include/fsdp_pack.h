@@ -34,11 +34,14 @@
  *     BF16, 4 for FP32); the all-gather byte buffers must be 16-byte aligned.
  *     A pointer may be NULL only if the tensor it stands for has 0 bytes.
  *   - Calls are asynchronous on the given stream (NULL = legacy default
- *     stream) and never synchronise the host.  Inputs must stay alive and
+ *     stream) and never synchronise the host (one exception:
+ *     fsdp_pack_reduce_scatter_noalloc may wait for its table copy to leave
+ *     the host, see there).  Inputs must stay alive and
  *     unmodified until the stream has passed the call.  Inputs and outputs
  *     must not overlap (undefined otherwise).
- *   - Calls allocate no device memory: the only device allocation is the work
- *     table made once by fsdp_plan_layout and freed by fsdp_layout_destroy.
+ *   - The per-call entry points allocate no device memory: the only device
+ *     allocation is the work table that fsdp_plan_layout makes once and
+ *     fsdp_layout_destroy frees.
  *   - Arguments are checked on the host before anything is launched.  On any
  *     error nothing is launched, the status says why, and fsdp_last_error()
  *     returns a one-line description for the calling thread.
@@ -341,14 +344,23 @@ fsdp_status_t fsdp_reduce_scatter_copy_out_batched(const fsdp_layout_t *const *l
  *   grads, bucket_bufs, stream: as for fsdp_pack_reduce_scatter.
  * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call
  * on a device looks up the array's device address and the grid size for that
- * device (cudaGetSymbolAddress, device queries); make that first call before
- * any stream capture.  Each call copies the work table into the array with
+ * device (cudaGetSymbolAddress, device queries).  The CUDA runtime loads a
+ * library's device code lazily by default, so that first call may also be
+ * what loads this library's module onto the device, and with it reserves
+ * the 4 MiB array and the module's code: make the first call at start-up,
+ * before the device memory is handed out to others and before any stream
+ * capture.  Each call copies the work table into the array with
  * cudaMemcpyAsync from the layout's host memory and clears the status word
- * there.  Every call shares the one array: calls whose work overlaps on the
- * GPU (on different streams, or from different threads) race and corrupt
- * each other's tables; order them on one stream.  A bounded device wait that
- * gives up in this variant records its status bit in the array and is not
- * read back.
+ * there.  That host memory is pageable, so the driver stages the copy and may
+ * hold the call until the table has left the host (or until earlier work on
+ * the stream is done): unlike the other entry points, this one can block the
+ * calling thread.  The kernel then launches in plain stream order, after
+ * everything queued before it on the stream.
+ * Every call shares the one array: calls whose work overlaps on the GPU (on
+ * different streams, or from different threads) race and corrupt each
+ * other's tables; order them on one stream.  A bounded device wait that gives
+ * up in this variant records its status bit in the array and is not read
+ * back.
  */
 fsdp_status_t fsdp_pack_reduce_scatter_noalloc(const fsdp_layout_t *L, const void *const *grads,
                                                void *const *bucket_bufs, fsdp_stream_t stream);
@@ -402,6 +414,18 @@ typedef enum {
   FSDP_SCHEDULE_MIXED = 3
 } fsdp_schedule_t;
 fsdp_status_t fsdp_debug_set_schedule(int32_t mode);
+
+/*
+ * Measurement utility, not a step of the method: a plain streaming widen of
+ * n BF16 elements to FP32 (each FP32 result is the BF16 bits shifted up by
+ * 16, exact), which moves bytes at the reduce-scatter pack's own 1 : 2 mix
+ * of bytes read to bytes written.  Benchmarks time it beside the pack as a
+ * same-machine reference for what a plain kernel reaches at that mix.
+ *   src: n BF16 elements, dst: n FP32 elements (device pointers, both
+ *   16-byte aligned, not overlapping); n a multiple of 8 (FSDP_EINVAL
+ *   otherwise).  n = 0 launches nothing.  Asynchronous on `stream`.
+ */
+fsdp_status_t fsdp_debug_stream_widen(const void *src, int64_t n, void *dst, fsdp_stream_t stream);
 
 /*
  * Test hook, process-wide.  While fail_upload is non-zero, planning with a

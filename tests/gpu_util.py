@@ -20,10 +20,11 @@ class DevBuf:
     aligned address, with GUARD canary bytes on both sides.  Everything,
     including the payload, starts as FILL so unwritten bytes show up."""
 
-    def __init__(self, nbytes: int, offset: int = 0, data: np.ndarray | None = None):
+    def __init__(self, nbytes: int, offset: int = 0, data: np.ndarray | None = None, fill: int = FILL):
         self.nbytes = int(nbytes)
         self.off = GUARD + int(offset)
-        self.raw = torch.full((self.off + self.nbytes + GUARD,), FILL, dtype=torch.uint8, device="cuda")
+        self.fill = fill
+        self.raw = torch.full((self.off + self.nbytes + GUARD,), fill, dtype=torch.uint8, device="cuda")
         assert self.raw.data_ptr() % 512 == 0
         if data is not None:
             self.write(data)
@@ -44,7 +45,7 @@ class DevBuf:
     def guards_ok(self) -> bool:
         head = self.raw[:self.off]
         tail = self.raw[self.off + self.nbytes:]
-        return bool((head == FILL).all().item()) and bool((tail == FILL).all().item())
+        return bool((head == self.fill).all().item()) and bool((tail == self.fill).all().item())
 
 
 def _offset(rng, align: int) -> int:
@@ -86,11 +87,11 @@ class GroupRun:
         self.L.close()
 
     # -- reduce-scatter copy-in --------------------------------------------
-    def pack(self):
+    def pack(self, fill: int = FILL):
         fp, pl = self.fp, self.pl
         g_bufs = [DevBuf(g.nbytes, _offset(self.rng, ESZ[s.grad_dtype]), g) for s, g in zip(self.specs, self.grads)]
         rho = ["f32" if d == oracle.F32 else "bf16" for d in pl.bucket_dtype]
-        out = [DevBuf(self.W * S * ESZ[r], _offset(self.rng, ESZ[r])) for r, S in zip(rho, pl.bucket_S)]
+        out = [DevBuf(self.W * S * ESZ[r], _offset(self.rng, ESZ[r]), fill=fill) for r, S in zip(rho, pl.bucket_S)]
         fp.fsdp_pack_reduce_scatter(self.L, [b.ptr for b in g_bufs], [b.ptr for b in out])
         fp.fsdp_sync_status(self.L)
         got = [b.read(NP[r]) for b, r in zip(out, rho)]

@@ -261,3 +261,13 @@ def test_schedule_hook_accepts_its_modes_and_refuses_others(fp):
         with pytest.raises(fp.FsdpError) as e:
             fp.fsdp_debug_set_schedule(bad)
         assert e.value.status == fp.FSDP_EINVAL and "unknown schedule mode" in str(e.value)
+
+
+def test_stream_widen_checks_its_arguments_without_launching(fp):
+    fp.fsdp_debug_stream_widen(0, 0, 0, stream=0)  # n = 0: nothing to do, no CUDA call
+    for src, n, dst, why in ((0x1000, 12, 0x100000, "multiple of 8"), (0x1000, -8, 0x100000, "multiple of 8"),
+                             (0x1008, 16, 0x100000, "16-byte aligned"), (0x1000, 16, 0x100004, "16-byte aligned"),
+                             (0, 16, 0x100000, "NULL"), (0x1000, 64, 0x1040, "overlap")):
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_debug_stream_widen(src, n, dst, stream=0)
+        assert e.value.status == fp.FSDP_EINVAL and why in str(e.value), (src, n, dst)

@@ -73,3 +73,29 @@ def test_reference_arm_runs_on_rank_0_only(capsys, monkeypatch):
     monkeypatch.setenv("LOCAL_RANK", "1")
     bench.main(["--impl", "reference", "--gpus", "2", "--steps", "40", "--warmup", "2"])
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_reference_arm_config_equals_our_arms(capsys):
+    """Both arms print the same `config` for the same flags.  The reference arm
+    takes the pack's bytes from the oracle's plan; ours takes them from the C
+    planner's layout (planned here on the host), so this also checks that the
+    two agree on the bytes the metric is computed from."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    from fsdp2_gradient_packing_gb300 import _build
+    _build.build()
+    from fsdp2_gradient_packing_gb300 import fsdp_pack as fp
+    bench.main(["--impl", "reference", "--steps", "10", "--warmup", "1"])
+    d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    args = bench.parse_args([])
+    factory, description = bench.WORKLOADS[args.workload]
+    work = factory()
+    specs = work.groups[0]
+    with fp.fsdp_plan_layout_host(specs, work.W) as L:
+        info = fp.fsdp_layout_query(L)
+        bucket_bytes = [fp.fsdp_layout_bucket(L, b).bytes for b in range(info.n_buckets)]
+        pack = bench.op_bytes(specs, work.W, bucket_bytes, info.ag_bytes)["pack"]
+    assert pack == 302_055_424
+    assert d["config"] == bench.make_config(args, work, description, 1, 1, pack, 1)

@@ -119,22 +119,26 @@ def _sample_indices(pl, b, rng, n_random):
 
 @pytest.mark.parametrize("W,reduce", [(8, "f32"), (64, "f32"), (8, "grad"), (64, "grad"), (8, "bf16")])
 def test_kda_block_full_size(fp, W, reduce):
-    """One block of the 1.75B-parameter KDA-style layout at full size.  The
-    pack output (up to 872 MB) is checked on sampled elements computed one by
-    one by the oracle, including every run's edges; the all-gather copy-in and
-    copy-out are compared whole."""
+    """One block of the 1.75B-parameter KDA-style layout at full size, in the
+    launch configuration the benchmark times.  Every bucket of the pack (up
+    to 872 MB) is compared whole with the oracle's pack, element by element.
+    At W = 64 the FP32 bucket row holds an odd number of elements, so every
+    rank's row starts at a different 16-byte phase and most items take the
+    shifted path.  The pack runs twice, into buffers pre-filled with two
+    different bytes, and both must equal the oracle: every output byte was
+    written.  The all-gather copy-in and copy-out are compared whole too."""
     work = wl.kda_block(W=W, reduce=reduce)
     specs = work.groups[0]
     run = GroupRun(fp, specs, W, work, 0)
     try:
-        got, ok = run.pack()
-        assert ok
-        rng = np.random.default_rng(W)
-        for b in range(len(got)):
-            idx = _sample_indices(run.pl, b, rng, 2_000_000)
-            want = oracle.pack_samples(run.pl, run.grads, b, idx)
-            assert np.array_equal(got[b][idx], want), f"bucket {b}: {first_mismatch(got[b][idx], want)}"
-        del got
+        want = run.pack_expected()
+        for fill in (0xA5, 0x5A):
+            got, ok = run.pack(fill=fill)
+            assert ok
+            for b, (x, y) in enumerate(zip(got, want)):
+                assert np.array_equal(x, y), f"fill {fill:#x}, bucket {b}: {first_mismatch(x, y)}"
+            del got
+        del want
         got, ok = run.rs_copy_out()
         assert ok
         for x, y in zip(got, run.rs_copy_out_expected()):
@@ -777,3 +781,20 @@ def test_device_table_allocation_failure_reports_enomem(fp):
             assert fp.fsdp_layout_query(L).has_device_table
     finally:
         run.close()
+
+
+def test_stream_widen_matches_oracle(fp):
+    """The plain BF16 -> FP32 streaming widen that the benchmark times beside
+    the pack: every BF16 bit pattern, then a seeded array long enough for
+    several grid-stride rounds, against the oracle's widening."""
+    every = np.arange(65536, dtype=np.uint16)
+    big = wl.normal_bits(152 * 32 * 256 * 8 * 3 + 8, "bf16", 1.0, 77, 1)
+    wl.inject_specials(big, "bf16", 0.01, 77, 2)
+    for bits in (every, big):
+        src = torch.from_numpy(bits.view(np.int16).copy()).cuda()
+        dst = torch.full((bits.size,), -1, dtype=torch.int32, device="cuda")
+        fp.fsdp_debug_stream_widen(src, bits.size, dst)
+        torch.cuda.synchronize()
+        got = dst.cpu().numpy().view(np.uint32)
+        want = oracle.bf16_to_f32(bits)
+        assert np.array_equal(got, want), first_mismatch(got, want)
