@@ -131,6 +131,8 @@ def parse_args(argv=None):
                     help="whole steps of the pass with CUDA events around every launch (per-operation times)")
     ap.add_argument("--reference-iters", type=int, default=400,
                     help="iterations of the same-run plain copies of the pack's bytes (0 = skip)")
+    ap.add_argument("--op-seconds", type=float, default=0.2,
+                    help="seconds of back-to-back launches per operation for ops_alone (0 = skip)")
     ap.add_argument("--no-extra", dest="extra", action="store_false",
                     help="skip the extra workloads (transformer layout batched, one KDA block at W = 64)")
     return ap.parse_args(argv)
@@ -462,6 +464,7 @@ class DeviceSet:
         self.shards = to_device(flatten(shards[rank_row], soffs, stot, torch), torch)
         self.shard_ptrs = fp.pointer_array([self.shards.data_ptr() + o for o in soffs])
         self.gathered = torch.empty(W * self.S_ag, dtype=torch.uint8, device=dev)
+        self.gathered_ptr = self.gathered.data_ptr()
         self.row_ptr = self.gathered.data_ptr() + rank_row * self.S_ag
         f_sizes = [s.numel * ESZ[s.param_dtype] for s in specs]
         foffs, ftot = flat_offsets(f_sizes)
@@ -497,29 +500,29 @@ class DeviceSet:
     def pack(self, fp, L, h):
         fp.fsdp_pack_reduce_scatter(L, self.grad_ptrs, self.bucket_ptrs, h)
 
+    def emulated_rs(self, fp, L, h):
+        fp.fsdp_emulated_reduce_scatter(L, self.packed_ptrs, self.reduced_ptrs, h)
+
+    def copy_in(self, fp, L, h):
+        fp.fsdp_allgather_copy_in(L, self.shard_ptrs, self.row_ptr, h)
+
+    def copy_out(self, fp, L, h):
+        fp.fsdp_allgather_copy_out(L, self.gathered_ptr, self.full_ptrs, h)
+
+    def rs_copy_out(self, fp, L, h):
+        fp.fsdp_reduce_scatter_copy_out(L, self.row0_ptrs, self.sharded_ptrs, h)
+
     def step(self, fp, L, h, ev=None, rs=False):
         """pack, [emulated reduce-scatter], copy-in, copy-out, [rs copy-out];
         ev[k] is recorded after the k-th launch (ev[0] before the first)."""
-        k = 0
-
-        def mark():
-            nonlocal k
+        ops = ["pack"] + (["emulated_rs"] if self.reduced is not None else []) + ["copy_in", "copy_out"] \
+            + (["rs_copy_out"] if rs else [])
+        for k, op in enumerate(ops):
             if ev is not None:
                 ev[k].record()
-            k += 1
-        mark()
-        fp.fsdp_pack_reduce_scatter(L, self.grad_ptrs, self.bucket_ptrs, h)
-        mark()
-        if self.reduced is not None:
-            fp.fsdp_emulated_reduce_scatter(L, self.packed_ptrs, self.reduced_ptrs, h)
-            mark()
-        fp.fsdp_allgather_copy_in(L, self.shard_ptrs, self.row_ptr, h)
-        mark()
-        fp.fsdp_allgather_copy_out(L, self.gathered.data_ptr(), self.full_ptrs, h)
-        mark()
-        if rs:
-            fp.fsdp_reduce_scatter_copy_out(L, self.row0_ptrs, self.sharded_ptrs, h)
-            mark()
+            getattr(self, op)(fp, L, h)
+        if ev is not None:
+            ev[len(ops)].record()
 
 
 class Group:
@@ -561,23 +564,26 @@ class Batch:
         a = self.sets[k]
         fp.fsdp_pack_reduce_scatter_batched(self.layouts, a["grads"], a["buckets"], h)
 
-    def step(self, fp, h, k, ev=None, rs=False):
+    def copy_in(self, fp, h, k):
         a = self.sets[k]
-        if ev is not None:
-            ev[0].record()
-        fp.fsdp_pack_reduce_scatter_batched(self.layouts, a["grads"], a["buckets"], h)
-        if ev is not None:
-            ev[1].record()
         fp.fsdp_allgather_copy_in_batched(self.layouts, a["shards"], a["rows"], h)
-        if ev is not None:
-            ev[2].record()
+
+    def copy_out(self, fp, h, k):
+        a = self.sets[k]
         fp.fsdp_allgather_copy_out_batched(self.layouts, a["gathered"], a["full"], h)
-        if ev is not None:
-            ev[3].record()
-        if rs:
-            fp.fsdp_reduce_scatter_copy_out_batched(self.layouts, a["row0"], a["sharded"], h)
+
+    def rs_copy_out(self, fp, h, k):
+        a = self.sets[k]
+        fp.fsdp_reduce_scatter_copy_out_batched(self.layouts, a["row0"], a["sharded"], h)
+
+    def step(self, fp, h, k, ev=None, rs=False):
+        ops = ["pack", "copy_in", "copy_out"] + (["rs_copy_out"] if rs else [])
+        for j, op in enumerate(ops):
             if ev is not None:
-                ev[4].record()
+                ev[j].record()
+            getattr(self, op)(fp, h, k)
+        if ev is not None:
+            ev[len(ops)].record()
 
 
 def precast_comparison(fp, torch, work, grp, h, iters, rows=False):
@@ -670,13 +676,31 @@ def same_run_references(fp, torch, pack_bytes, iters):
             "iters": iters}
 
 
-def run_packs(fp, groups, h, first, count, batch=None):
+def run_packs(fp, groups, h, first, count, batch=None, op="pack"):
+    """`count` calls of one operation (default the pack) for every group,
+    alternating the two buffer sets."""
     for i in range(first, first + count):
         if batch is not None:
-            batch.pack(fp, h, i & 1)
+            getattr(batch, op)(fp, h, i & 1)
             continue
         for grp in groups:
-            grp.sets[i & 1].pack(fp, grp.L, h)
+            getattr(grp.sets[i & 1], op)(fp, grp.L, h)
+
+
+def ops_alone(fp, torch, groups, batch, h, OPS, nbytes, n_launch, seconds):
+    """Each operation alone: launches of that operation back to back
+    (alternating the buffer sets, no events between them), about `seconds`
+    of each after a short estimate."""
+    out = {}
+    for op in OPS:
+        est = loop_ms(torch, lambda k: run_packs(fp, groups, h, k, 1, batch, op), 20)
+        iters = max(50, int(seconds / (est * 1e-3)))
+        ms = loop_ms(torch, lambda k: run_packs(fp, groups, h, k, 1, batch, op), iters)
+        out[op] = {"bytes": nbytes[op], "launches_per_call": n_launch, "calls": iters, "us": ms * 1e3,
+                   "gbs": nbytes[op] / (ms * 1e-3) / 1e9}
+    for grp in groups:
+        fp.fsdp_sync_status(grp.L)
+    return out
 
 
 def run_steps(fp, groups, h, first, count, evs=None, batch=None, rs=False):
@@ -802,6 +826,8 @@ def run_ours(args):
     pack_total_ms, step_total_ms, clocks = timed_passes(fp, torch, groups, batch, h, K, args.warmup, rs,
                                                         args.graph, gpu_id)
     per = evented_ops(fp, torch, groups, batch, h, min(K, args.evented_steps), OPS, rs)
+    alone = ops_alone(fp, torch, groups, batch, h, OPS, nbytes, n_launch, args.op_seconds) \
+        if args.op_seconds > 0 else None
 
     refs = same_run_references(fp, torch, nbytes["pack"], args.reference_iters) if args.reference_iters > 0 else None
     precast = None
@@ -824,6 +850,10 @@ def run_ours(args):
     if rank == 0:
         result = report(args, work, description, groups, nbytes, step_bytes, pack_total_ms, step_total_ms, per,
                         clocks, e2e, step_e2e, n_launch, world, K, refs)
+        if alone is not None:
+            result["ops_alone"] = alone
+            result["ops_alone_note"] = ("each operation alone, its launches back to back with no events between "
+                                        "them (programmatic dependent launch on): per-call device time")
         if precast is not None:
             result["precast_baseline"] = precast
         if extra is not None:
@@ -860,6 +890,7 @@ def run_extra(fp, torch, h, wname, batched, gpu_id, seconds=0.5):
     K += K & 1
     pack_ms, step_ms, clocks = timed_passes(fp, torch, groups, batch, h, K, 10, False, False, gpu_id)
     per = evented_ops(fp, torch, groups, batch, h, min(K, 500), OPS, False)
+    alone = ops_alone(fp, torch, groups, batch, h, OPS, nbytes, n_launch, 0.1)
     peak, peak_kind = read_peaks()
     pack_gbs = nbytes["pack"] * K / (pack_ms * 1e-3) / 1e9
     out = {"workload": description, "groups": len(groups), "launches_per_op": n_launch, "steps": K,
@@ -867,7 +898,7 @@ def run_extra(fp, torch, h, wname, batched, gpu_id, seconds=0.5):
                     "frac_of_nominal_8tbs": pack_gbs / NOMINAL_HBM_GBS, "peak": peak, "peak_source": peak_kind},
            "hot_path_step": {"bytes": step_bytes, "us": step_ms * 1e3 / K,
                              "gbs": step_bytes * K / (step_ms * 1e-3) / 1e9},
-           "ops": op_rows(nbytes, per, n_launch), "clocks": clocks}
+           "ops": op_rows(nbytes, per, n_launch), "ops_alone": alone, "clocks": clocks}
     for grp in groups:
         grp.L.close()
     del groups, batch
@@ -1014,7 +1045,8 @@ def report(args, work, description, groups, nbytes, step_bytes, pack_total_ms, s
                           "timing": "K whole steps back to back right after the timed region, same clocks"},
         "ops": op_rows(nbytes, per, n_launch),
         "ops_note": "per-operation device times from a pass of whole steps with CUDA events around every "
-                    "launch (summed over the step's groups)",
+                    "launch (summed over the step's groups); events serialise the launches, and each operation "
+                    "also pays for the L2 write-back of the one before it",
         "roofline": roofline,
         "e2e": e2e,
         "hot_path_step_e2e": step_e2e,

@@ -68,16 +68,17 @@ constexpr int kStageDataBytes = (int)kStageBytes + 32;
 constexpr int kHeaderBytes = 64;
 constexpr int kStageStride = (kStageDataBytes + kHeaderBytes + 127) / 128 * 128;
 static_assert(kStageDataBytes % 16 == 0, "stage header must stay 16-byte aligned");
-// After the stages and their barriers: the resolved headers of a CTA's first
-// kPrefetch items (StageHeader, 32 bytes each), then, for batched launches,
-// the layouts' first global item indices (kMaxBatch + 1 int64).
+// After the stages: their "full" and "empty" barriers, then the resolved
+// headers of a CTA's first kPrefetch items (StageHeader, 32 bytes each; see
+// the producer prologue).  The prologue runs in launches of at most
+// kPrologueMaxRounds items per CTA.
 constexpr int kPrefetch = 32;
-constexpr int kMaxBatch = 64;
+constexpr int64_t kPrologueMaxRounds = 64;
+constexpr int kMaxBatch = 64;  // layouts in one batched launch
 constexpr int kBarrierBytes = 2 * kStages * 8;
 constexpr int kPrefetchOffset = kStages * kStageStride + kBarrierBytes;
-constexpr int kStartOffset = kPrefetchOffset + kPrefetch * 32;
-constexpr int kSmemBytes = kStartOffset + (kMaxBatch + 1) * 8;
-static_assert(kPrefetchOffset % 16 == 0 && kStartOffset % 16 == 0, "shared tables must stay 16-byte aligned");
+constexpr int kSmemBytes = kPrefetchOffset + kPrefetch * 32;
+static_assert(kPrefetchOffset % 16 == 0, "shared tables must stay 16-byte aligned");
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 // Status bits written by a kernel whose bounded wait gave up.
@@ -108,10 +109,12 @@ constexpr int32_t kSchedMixed = 1;
 // Per-call pointers travel by value in the parameter block: `slot` is read
 // with a run-time index, which __grid_constant__ allows without a local copy.
 // fetch(i) returns work item i and the slot base its slot numbers are
-// relative to; `cursor` carries the layout of the CTA's previous item and
-// `tab` is the launch's table in shared memory (see prepare).
+// relative to; `cursor` carries the layout of the CTA's previous item.
 template <int NSLOT>
 struct LaunchArgs {
+  // The producer warp's lanes resolve the CTA's first items in parallel
+  // (see the producer prologue in walk_kernel).
+  static constexpr bool kParallelPrologue = true;
   const WorkItem *items;
   int64_t n_items;
   uint32_t *status;
@@ -121,13 +124,7 @@ struct LaunchArgs {
   Sched sched;
   const void *slot[NSLOT];
 
-  // Nothing to copy into shared memory for a single layout.
-  __device__ __forceinline__ void prepare(int64_t *, int) const {}
-  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *, const int64_t *) const {
-    *base = 0;
-    return items[i];
-  }
-  __device__ __forceinline__ WorkItem fetch_any(int64_t i, int32_t *base, const int64_t *) const {
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *) const {
     *base = 0;
     return items[i];
   }
@@ -137,6 +134,12 @@ struct LaunchArgs {
 // [start[g], start[g+1]); their slots are numbered from slot_base[g].
 template <int NSLOT>
 struct BatchArgs {
+  // A batched launch resolves its items one at a time on the producer lane.
+  // Resolved by a warp's lanes at once, the lookups would index the
+  // per-layout arrays and the slots of the parameter block with a different
+  // index in every lane, which the constant cache serves one address after
+  // another: measured slower than the sequential producer.
+  static constexpr bool kParallelPrologue = false;
   int64_t n_items;
   uint32_t *status;
   uint64_t wait_limit_ns;
@@ -148,39 +151,18 @@ struct BatchArgs {
   int32_t slot_base[kMaxBatch];
   const void *slot[NSLOT];
 
-  // Warp 0 copies start[0 .. n_groups] into shared memory (`tab`), where the
-  // producer's lookups read it instead of the parameter block.
-  __device__ __forceinline__ void prepare(int64_t *tab, int lane) const {
-    for (int g = lane; g <= n_groups; g += 32) tab[g] = start[g];
-  }
-  __device__ __forceinline__ WorkItem at(int g, int64_t i, int32_t *base, const int64_t *tab) const {
-    *base = slot_base[g];
-    return items[g][i - tab[g]];
-  }
   // The last group that starts at or before i, found by walking forward
-  // from the CTA's previous one (`cursor`; -1 or a group past i: bisection
-  // first): a CTA's item indices grow, so the walk costs about one step per
-  // layout over the launch.
-  // The group of item i by bisection: the last group that starts at or
-  // before i (every group of the launch holds at least one item).
-  __device__ __forceinline__ int locate(int64_t i, const int64_t *tab) const {
-    int lo = 0, hi = n_groups - 1;  // tab[lo] <= i, and the answer is at most hi
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (tab[mid] <= i) lo = mid;
-      else hi = mid - 1;
-    }
-    return lo;
-  }
-  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *cursor, const int64_t *tab) const {
+  // from the CTA's previous one: a CTA's item indices grow (except after the
+  // rare retake of the work-sharing word, which restarts the walk), so the
+  // walk costs about one step per layout instead of a chain of dependent
+  // parameter loads per item.
+  __device__ __forceinline__ WorkItem fetch(int64_t i, int32_t *base, int *cursor) const {
     int g = *cursor;
-    if (g < 0 || tab[g] > i) g = locate(i, tab);
-    while (g + 1 < n_groups && tab[g + 1] <= i) ++g;
+    if (start[g] > i) g = 0;
+    while (g + 1 < n_groups && start[g + 1] <= i) ++g;
     *cursor = g;
-    return at(g, i, base, tab);
-  }
-  __device__ __forceinline__ WorkItem fetch_any(int64_t i, int32_t *base, const int64_t *tab) const {
-    return at(locate(i, tab), i, base, tab);
+    *base = slot_base[g];
+    return items[g][i - start[g]];
   }
 };
 
@@ -525,7 +507,6 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageStride);
   uint64_t *empty = full + kStages;
   StageHeader *pre = reinterpret_cast<StageHeader *>(smem + kPrefetchOffset);
-  int64_t *tab = reinterpret_cast<int64_t *>(smem + kStartOffset);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -541,25 +522,31 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     const int64_t G = gridDim.x, n = a.n_items;
     const Sched sc = a.sched;
     const int64_t shared0 = sc.word ? sc.fixed_rounds * G : 0;  // first shared item
-    // This CTA's fixed-order items are blockIdx.x + m * G below fixed_end
-    // (at least one: the grid is at most n, and a launch that shares items
-    // keeps at least one fixed round).  Before waiting for the previous
-    // kernel, the warp's lanes resolve the first kPrefetch of them at once --
-    // descriptor from the work table, source and destination pointers from
-    // the parameter block -- into `pre`.  Done by one thread, each item's
-    // lookups are a chain of dependent loads that miss the caches on a fresh
-    // launch, and that chain would sit between consecutive bulk copies.
+    // This CTA's fixed-order items are blockIdx.x + m * G below fixed_end (at
+    // least one: the grid is at most n, and a launch that shares items keeps
+    // at least one fixed round).  Prologue, before waiting for the previous
+    // kernel: in a single launch of at most kPrologueMaxRounds items per CTA,
+    // the warp's lanes resolve the first n_pre of them at once -- descriptor
+    // from the work table, source and destination pointers from the
+    // parameter block -- into `pre`.  Done by one thread, each item's lookups
+    // are a chain of dependent loads that miss the caches on a fresh launch,
+    // and the chain would sit between consecutive bulk copies.  A long
+    // launch keeps its pipeline full anyway and loses more by starting late
+    // (every lane's lookups must land before the first copy); a batched one
+    // resolves items one at a time (see BatchArgs).
     const int64_t fixed_end = sc.word ? (shared0 < n ? shared0 : n) : n;
     const int64_t n_fixed = (int64_t)blockIdx.x < fixed_end ? (fixed_end - blockIdx.x + G - 1) / G : 0;
-    const int n_pre = (int)(n_fixed < kPrefetch ? n_fixed : kPrefetch);
-    a.prepare(tab, lane);
-    __syncwarp();
-    if (lane < n_pre) {
-      int32_t base = 0;
-      const WorkItem w = a.fetch_any(blockIdx.x + (int64_t)lane * G, &base, tab);
-      pre[lane] = resolve_item(a, w, base);
+    const int n_pre = Args::kParallelPrologue && n <= kPrologueMaxRounds * G
+                          ? (int)(n_fixed < kPrefetch ? n_fixed : kPrefetch) : 0;
+    if (n_pre > 0) {
+      if (lane < n_pre) {
+        int cur = 0;
+        int32_t base = 0;
+        const WorkItem w = a.fetch(blockIdx.x + (int64_t)lane * G, &base, &cur);
+        pre[lane] = resolve_item(a, w, base);
+      }
+      __syncwarp();
     }
-    __syncwarp();
     if (lane != 0) return;
     // Producer (lane 0).  Item indices are claimed two items ahead of use,
     // and the descriptors of items past the prefetched ones are fetched one
@@ -607,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     };
     int64_t k = 0;
     bool skipped_first = false, stopped = false;
-    int cursor = -1;  // layout of the last fetched item (batched launches; -1: none yet)
+    int cursor = 0;  // layout of the last fetched item (batched launches)
     // Stage the item with resolved header h in the ring; false if the stage
     // never came free (the wait gave up).
     auto stage_item = [&](const StageHeader &h) -> bool {
@@ -637,6 +624,16 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       ++k;
       return true;
     };
+    // Item 0 (blockIdx.x in every schedule: the grid is at most n) is
+    // resolved before waiting for the previous kernel on the stream.
+    StageHeader h0;
+    if (n_pre > 0) {
+      h0 = pre[0];
+    } else {
+      int32_t base0 = 0;
+      const WorkItem w0 = a.fetch(blockIdx.x, &base0, &cursor);
+      h0 = resolve_item(a, w0, base0);
+    }
     wait_for_previous_grid();
     if (!sc.word) {
       // Fixed order: items blockIdx.x + mi * G; past the prefetched ones,
@@ -644,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       WorkItem nxt{};
       int32_t nxt_base = 0;
       for (int64_t i = blockIdx.x, mi = 0; i < n; i += G, ++mi) {
-        const StageHeader h = mi < n_pre ? pre[mi] : resolve_item(a, nxt, nxt_base);
-        if (mi + 1 >= n_pre && i + G < n) nxt = a.fetch(i + G, &nxt_base, &cursor, tab);
+        const StageHeader h = mi == 0 ? h0 : mi < n_pre ? pre[mi] : resolve_item(a, nxt, nxt_base);
+        if (mi + 1 >= n_pre && i + G < n) nxt = a.fetch(i + G, &nxt_base, &cursor);
         if (!stage_item(h)) {
           stopped = true;
           break;
@@ -654,12 +651,13 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     } else {
       // Shared: each round issues the claim two items ahead and takes the
       // one issued the round before (a first round only primes that queue).
-      // Item c0 is in hand: prefetched (c0_pm >= 0) or its descriptor
-      // fetched.  Joining the word comes after the wait above, when an
-      // earlier launch of the same operation on the stream has let go of it.
+      // Item c0 is in hand: item 0's header h0 (c0_pm == -2), a prefetched
+      // header (c0_pm >= 0) or a fetched descriptor (c0_pm == -1).  Joining
+      // the word comes after the wait above, when an earlier launch of the
+      // same operation on the stream has let go of it.
       m = 1;
       int64_t c0 = blockIdx.x;
-      int32_t c0_pm = 0, c0_base = 0;
+      int32_t c0_pm = -2, c0_base = 0;
       WorkItem c0_w{};
       Claim q1{};
       bool primed = false;
@@ -670,11 +668,11 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
           primed = true;
           continue;
         }
-        const StageHeader h = c0_pm >= 0 ? pre[c0_pm] : resolve_item(a, c0_w, c0_base);
+        const StageHeader h = c0_pm == -2 ? h0 : c0_pm >= 0 ? pre[c0_pm] : resolve_item(a, c0_w, c0_base);
         const int64_t c1 = take(q1);
         if (c1 < n) {
           c0_pm = q1.pm;
-          if (c0_pm < 0) c0_w = a.fetch(c1, &c0_base, &cursor, tab);
+          if (c0_pm < 0) c0_w = a.fetch(c1, &c0_base, &cursor);
         }
         q1 = qn;
         c0 = c1;

@@ -271,3 +271,4 @@ def test_stream_widen_checks_its_arguments_without_launching(fp):
         with pytest.raises(fp.FsdpError) as e:
             fp.fsdp_debug_stream_widen(src, n, dst, stream=0)
         assert e.value.status == fp.FSDP_EINVAL and why in str(e.value), (src, n, dst)
+
