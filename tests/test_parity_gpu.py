@@ -798,3 +798,144 @@ def test_stream_widen_matches_oracle(fp):
         got = dst.cpu().numpy().view(np.uint32)
         want = oracle.bf16_to_f32(bits)
         assert np.array_equal(got, want), first_mismatch(got, want)
+
+
+def test_entry_points_replay_from_a_cuda_graph(fp):
+    """Every per-call entry point captured in one CUDA graph and replayed:
+    the pack, the reduce-scatter copy-out, the copy-in of every rank, the
+    copy-out and a batched pack of two layouts.  Each replay writes outputs
+    refilled with a different byte beforehand, and each must equal the
+    oracle: the launches (with their programmatic dependent launch edges)
+    are recorded with their arguments and replay exactly."""
+    work = wl.transformer_500(W=8, layers=2)
+    runs = [GroupRun(fp, specs, work.W, work, g, misalign_seed=g + 7, specials=0.02)
+            for g, specs in enumerate(work.groups)]
+    try:
+        r0 = runs[0]
+        rho = ["f32" if d == oracle.F32 else "bf16" for d in r0.pl.bucket_dtype]
+        g_bufs = [DevBuf(g.nbytes, 0, g) for g in r0.grads]
+        buckets = [DevBuf(r0.W * S * ESZ[r], 0) for r, S in zip(rho, r0.pl.bucket_S)]
+        rows = [DevBuf(x.nbytes, 0, x) for x in r0.rows]
+        sharded = [DevBuf(c * ESZ[s.shard_dtype], 0) for s, c in zip(r0.specs, r0.pl.chunk)]
+        shard_bufs = [[DevBuf(x.nbytes, 0, x) for x in r0.shards[r]] for r in range(r0.W)]
+        gathered = DevBuf(r0.W * r0.pl.S_ag, 0)
+        full = [DevBuf(s.numel * ESZ[s.param_dtype], 0) for s in r0.specs]
+        r1 = runs[1]
+        g1 = [DevBuf(g.nbytes, 0, g) for g in r1.grads]
+        b_batched = [[DevBuf(run.W * S * ESZ[r], 0) for r, S in zip(rho, run.pl.bucket_S)] for run in (r0, r1)]
+        outputs = buckets + sharded + [gathered] + full + [b for bs in b_batched for b in bs]
+
+        def record():
+            fp.fsdp_pack_reduce_scatter(r0.L, [b.ptr for b in g_bufs], [b.ptr for b in buckets])
+            fp.fsdp_reduce_scatter_copy_out(r0.L, [b.ptr for b in rows], [b.ptr for b in sharded])
+            for r in range(r0.W):
+                fp.fsdp_allgather_copy_in(r0.L, [b.ptr for b in shard_bufs[r]], gathered.ptr + r * r0.pl.S_ag)
+            fp.fsdp_allgather_copy_out(r0.L, gathered.ptr, [b.ptr for b in full])
+            fp.fsdp_pack_reduce_scatter_batched([r0.L, r1.L], [b.ptr for b in g_bufs] + [b.ptr for b in g1],
+                                                [b.ptr for bs in b_batched for b in bs])
+
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            record()
+        want_b = r0.pack_expected()
+        want_b1 = r1.pack_expected()
+        want_sh = r0.rs_copy_out_expected()
+        want_rows, want_full = r0.gather_expected()
+        for fill in (0x5A, 0xC3):
+            for b in outputs:
+                b.raw[b.off:b.off + b.nbytes].fill_(fill)
+            graph.replay()
+            torch.cuda.synchronize()
+            fp.fsdp_sync_status(r0.L)
+            for b, (buf, want, r) in enumerate(zip(buckets, want_b, rho)):
+                got = buf.read(NP[r])
+                assert np.array_equal(got, want), f"fill {fill:#x} pack bucket {b}: {first_mismatch(got, want)}"
+            for p, (buf, s, want) in enumerate(zip(sharded, r0.specs, want_sh)):
+                got = buf.read(NP[s.shard_dtype])
+                assert np.array_equal(got, want), f"fill {fill:#x} rs copy-out {p}: {first_mismatch(got, want)}"
+            got = gathered.read()
+            assert np.array_equal(got, want_rows), f"fill {fill:#x} copy-in: {first_mismatch(got, want_rows)}"
+            for p, (buf, s, want) in enumerate(zip(full, r0.specs, want_full)):
+                got = buf.read(NP[s.param_dtype])
+                assert np.array_equal(got, want), f"fill {fill:#x} copy-out {p}: {first_mismatch(got, want)}"
+            for n, (bs, wants) in enumerate(zip(b_batched, (want_b, want_b1))):
+                for b, (buf, want, r) in enumerate(zip(bs, wants, rho)):
+                    got = buf.read(NP[r])
+                    assert np.array_equal(got, want), f"fill {fill:#x} batched {n} bucket {b}: {first_mismatch(got, want)}"
+            assert all(b.guards_ok() for b in outputs)
+        del graph
+    finally:
+        for run in runs:
+            run.close()
+
+
+def test_one_layout_from_several_host_threads_and_streams(fp):
+    """Four host threads share one layout, each with its own stream and
+    buffers, and pack, copy in and copy out over and over at once (the C
+    calls run without the Python lock, so they enter the library together;
+    the launches overlap on the GPU and contend for the layout's
+    work-sharing words).  Every thread's final outputs must equal the
+    oracle's, and a host-side argument error raised in one thread must not
+    leak into another thread's error message."""
+    import threading
+
+    work = wl.mixed_50m(W=8, layers=2)  # the pack's 6,176 items share their last quarter through a word
+    specs, W = work.groups[0], work.W
+    run = GroupRun(fp, specs, W, work, 0, specials=0.01)
+    try:
+        rho = ["f32" if d == oracle.F32 else "bf16" for d in run.pl.bucket_dtype]
+        want_b = run.pack_expected()
+        want_rows, want_full = run.gather_expected()
+        g_bufs = [DevBuf(g.nbytes, 0, g) for g in run.grads]
+        shard_bufs = [[DevBuf(x.nbytes, 0, x) for x in run.shards[r]] for r in range(W)]
+        n_threads, iters = 4, 12
+        outs = []
+        for t in range(n_threads):
+            outs.append(dict(buckets=[DevBuf(W * S * ESZ[r], 0) for r, S in zip(rho, run.pl.bucket_S)],
+                             gathered=DevBuf(W * run.pl.S_ag, 0),
+                             full=[DevBuf(s.numel * ESZ[s.param_dtype], 0) for s in specs],
+                             stream=torch.cuda.Stream()))
+        errors = []
+        torch.cuda.synchronize()
+
+        def worker(t):
+            try:
+                o = outs[t]
+                for k in range(iters):
+                    fp.fsdp_pack_reduce_scatter(run.L, [b.ptr for b in g_bufs], [b.ptr for b in o["buckets"]],
+                                                o["stream"])
+                    for r in range(W):
+                        fp.fsdp_allgather_copy_in(run.L, [b.ptr for b in shard_bufs[r]],
+                                                  o["gathered"].ptr + r * run.pl.S_ag, o["stream"])
+                    fp.fsdp_allgather_copy_out(run.L, o["gathered"].ptr, [b.ptr for b in o["full"]], o["stream"])
+                    if t == 1 and k % 3 == 0:  # a rejected call in one thread: 1-byte misaligned bucket
+                        try:
+                            fp.fsdp_pack_reduce_scatter(run.L, [b.ptr for b in g_bufs],
+                                                        [o["buckets"][0].ptr + 1], o["stream"])
+                            errors.append("misaligned bucket was accepted")
+                        except fp.FsdpError as e:
+                            if "bucket_bufs[0] is not 4-byte aligned" not in str(e):
+                                errors.append(f"wrong error text: {e}")
+                fp.fsdp_sync_status(run.L, o["stream"])
+            except Exception as e:  # noqa: BLE001 - reported below
+                errors.append(f"thread {t}: {e!r}")
+
+        threads = [threading.Thread(target=worker, args=(t,)) for t in range(n_threads)]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        torch.cuda.synchronize()
+        assert not errors, errors
+        for t, o in enumerate(outs):
+            for b, (buf, want, r) in enumerate(zip(o["buckets"], want_b, rho)):
+                got = buf.read(NP[r])
+                assert np.array_equal(got, want), f"thread {t} bucket {b}: {first_mismatch(got, want)}"
+            got = o["gathered"].read()
+            assert np.array_equal(got, want_rows), f"thread {t} copy-in: {first_mismatch(got, want_rows)}"
+            for p, (buf, s, want) in enumerate(zip(o["full"], specs, want_full)):
+                got = buf.read(NP[s.param_dtype])
+                assert np.array_equal(got, want), f"thread {t} copy-out {p}: {first_mismatch(got, want)}"
+    finally:
+        run.close()
