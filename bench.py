@@ -309,14 +309,17 @@ def flat_offsets(sizes, align=256):
     return offs, max(at, align)
 
 
-def host_inputs(work, g, rows=False):
-    """Seeded gradients and every rank's shards of group g (host arrays)."""
+def host_inputs(work, g, rows=False, shards=True):
+    """Seeded gradients and (unless ``shards`` is False) every rank's shards
+    of group g (host arrays)."""
     specs, W = work.groups[g], work.W
     c = chunks(specs, W, rows)
     grads = [wl.grad_values(work, g, i) for i in range(len(specs))]
-    shards = [[wl.shard_values(work, g, i, r, c[i], max(0, min(c[i], s.numel - r * c[i])))
-               for i, s in enumerate(specs)] for r in range(W)]
-    return grads, shards
+    if not shards:
+        return grads, None
+    local = [[wl.shard_values(work, g, i, r, c[i], max(0, min(c[i], s.numel - r * c[i])))
+              for i, s in enumerate(specs)] for r in range(W)]
+    return grads, local
 
 
 def device_inputs(work, g, rows=False):
@@ -1067,7 +1070,7 @@ def run_reference(args):
         return
     factory, description = WORKLOADS[args.workload]
     work = factory()
-    inputs = [host_inputs(work, g, args.row_chunks) for g in range(len(work.groups))]
+    inputs = [host_inputs(work, g, args.row_chunks, shards=False) for g in range(len(work.groups))]
     samp = OracleSampler(work, inputs, args.row_chunks)
     for _ in range(args.warmup):
         samp.next()
