@@ -75,6 +75,13 @@ static_assert(kStageDataBytes % 16 == 0, "stage header must stay 16-byte aligned
 // kPrologueMaxRounds items per CTA.
 constexpr int kPrefetch = 32;
 constexpr int64_t kPrologueMaxRounds = 64;
+// Items per CTA whose staged source is prefetched into L2 before the
+// dependent-launch wait: the ones that fill the ring first.  Without the
+// parallel prologue the producer looks them up one after another, which pays
+// off only in launches of at least kSeqPrefetchMinRounds items per CTA; shorter
+// ones look up item 0 alone.
+constexpr int kL2PrefetchItems = kStages;
+constexpr int64_t kSeqPrefetchMinRounds = 16;
 constexpr int kMaxBatch = 64;  // layouts in one batched launch
 constexpr int kBarrierBytes = 2 * kStages * 8;
 constexpr int kPrefetchOffset = kStages * kStageStride + kBarrierBytes;
@@ -338,6 +345,21 @@ struct StageHeader {
 };
 static_assert(sizeof(StageHeader) <= kHeaderBytes, "stage header too large");
 static_assert(sizeof(StageHeader) == 32, "the prefetch table holds 32-byte headers");
+
+// Warm L2 with the staged source of the item with header h -- the 16-byte
+// blocks its bulk copy will read -- without waiting for it.  A prefetch is
+// only a hint into L2, which every SM sees coherently, so it may be issued
+// before the previous kernel on the stream has finished: the bulk copy after
+// griddepcontrol.wait still reads whatever that kernel wrote.  Issued by a
+// launch whose blocks start while the previous launch drains, it puts the
+// first reads in flight during that tail instead of after it.
+__device__ __forceinline__ void prefetch_item(const StageHeader &h) {
+  const int ss = (h.kind & 1) ? 2 : 4;
+  const Staged st = staged_of(h.src, h.n_copy * ss);
+  if (st.bytes > 0 && st.bytes <= kStagedMax)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(h.src - st.lead), "r"((uint32_t)st.bytes)
+                 : "memory");
+}
 constexpr int32_t kSkipItem = -1;
 constexpr int32_t kDoneItem = -2;  // no item follows: the consumers leave
 
@@ -537,14 +559,16 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     // resolves items one at a time (see BatchArgs).
     const int64_t fixed_end = sc.word ? (shared0 < n ? shared0 : n) : n;
     const int64_t n_fixed = (int64_t)blockIdx.x < fixed_end ? (fixed_end - blockIdx.x + G - 1) / G : 0;
-    const int n_pre = Args::kParallelPrologue && n <= kPrologueMaxRounds * G
-                          ? (int)(n_fixed < kPrefetch ? n_fixed : kPrefetch) : 0;
+    int n_pre = Args::kParallelPrologue && n <= kPrologueMaxRounds * G
+                    ? (int)(n_fixed < kPrefetch ? n_fixed : kPrefetch) : 0;
     if (n_pre > 0) {
       if (lane < n_pre) {
         int cur = 0;
         int32_t base = 0;
         const WorkItem w = a.fetch(blockIdx.x + (int64_t)lane * G, &base, &cur);
-        pre[lane] = resolve_item(a, w, base);
+        const StageHeader h = resolve_item(a, w, base);
+        pre[lane] = h;
+        if (lane < kL2PrefetchItems) prefetch_item(h);
       }
       __syncwarp();
     }
@@ -625,16 +649,22 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       ++k;
       return true;
     };
-    // Item 0 (blockIdx.x in every schedule: the grid is at most n) is
-    // resolved before waiting for the previous kernel on the stream.
-    StageHeader h0;
-    if (n_pre > 0) {
-      h0 = pre[0];
-    } else {
-      int32_t base0 = 0;
-      const WorkItem w0 = a.fetch(blockIdx.x, &base0, &cursor);
-      h0 = resolve_item(a, w0, base0);
+    // Without the parallel prologue, the producer resolves the items that fill
+    // the ring first (at least item 0: blockIdx.x in every schedule, the grid
+    // being at most n) one by one into `pre`, also before waiting for the
+    // previous kernel on the stream, and prefetches their sources.
+    if (n_pre == 0) {
+      const int64_t depth = n >= kSeqPrefetchMinRounds * G ? kL2PrefetchItems : 1;
+      const int64_t n_seq = n_fixed < depth ? n_fixed : depth;
+      for (int64_t mi = 0; mi < n_seq; ++mi) {
+        int32_t base = 0;
+        const WorkItem w = a.fetch(blockIdx.x + mi * G, &base, &cursor);
+        pre[mi] = resolve_item(a, w, base);
+        prefetch_item(pre[mi]);
+      }
+      n_pre = (int)n_seq;
     }
+    const StageHeader h0 = pre[0];
     wait_for_previous_grid();
     if (!sc.word) {
       // Fixed order: items blockIdx.x + mi * G; past the prefetched ones,
