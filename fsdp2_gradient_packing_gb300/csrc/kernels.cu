@@ -76,10 +76,11 @@ static_assert(kStageDataBytes % 16 == 0, "stage header must stay 16-byte aligned
 constexpr int kPrefetch = 32;
 constexpr int64_t kPrologueMaxRounds = 64;
 // Items per CTA whose staged source is prefetched into L2 before the
-// dependent-launch wait: the ones that fill the ring first.  Without the
-// parallel prologue the producer looks them up one after another, which pays
-// off only in launches of at least kSeqPrefetchMinRounds items per CTA; shorter
-// ones look up item 0 alone.
+// dependent-launch wait: the ones that fill the ring first, and only in a CTA
+// that has more fixed-order items than that to follow.  Without the parallel
+// prologue the producer looks them up one after another, which pays off only
+// in launches of at least kSeqPrefetchMinRounds items per CTA; shorter ones
+// look up (and prefetch) item 0 alone.
 constexpr int kL2PrefetchItems = kStages;
 constexpr int64_t kSeqPrefetchMinRounds = 16;
 constexpr int kMaxBatch = 64;  // layouts in one batched launch
@@ -352,7 +353,10 @@ static_assert(sizeof(StageHeader) == 32, "the prefetch table holds 32-byte heade
 // before the previous kernel on the stream has finished: the bulk copy after
 // griddepcontrol.wait still reads whatever that kernel wrote.  Issued by a
 // launch whose blocks start while the previous launch drains, it puts the
-// first reads in flight during that tail instead of after it.
+// first reads in flight during that tail instead of after it.  A CTA whose
+// whole work is those first items does not prefetch: when nothing overlaps
+// (a previous kernel that does not release its dependents early), a launch
+// whose every read waits behind its own prefetch was measured slower.
 __device__ __forceinline__ void prefetch_item(const StageHeader &h) {
   const int ss = (h.kind & 1) ? 2 : 4;
   const Staged st = staged_of(h.src, h.n_copy * ss);
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         const WorkItem w = a.fetch(blockIdx.x + (int64_t)lane * G, &base, &cur);
         const StageHeader h = resolve_item(a, w, base);
         pre[lane] = h;
-        if (lane < kL2PrefetchItems) prefetch_item(h);
+        if (n_fixed > kStages && lane < kL2PrefetchItems) prefetch_item(h);
       }
       __syncwarp();
     }
@@ -660,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         int32_t base = 0;
         const WorkItem w = a.fetch(blockIdx.x + mi * G, &base, &cursor);
         pre[mi] = resolve_item(a, w, base);
-        prefetch_item(pre[mi]);
+        if (n_fixed > kStages) prefetch_item(pre[mi]);
       }
       n_pre = (int)n_seq;
     }
