@@ -659,10 +659,14 @@ def loop_ms(torch, fn, iters, warm=10):
     return e0.elapsed_time(e1) / iters
 
 
-def same_run_references(fp, torch, pack_bytes, iters):
+def same_run_references(fp, torch, nbytes, iters):
     """Plain copies of the pack's byte count in the same process and loop
     style: the library's streaming BF16 -> FP32 widen (the pack's 1 : 2 mix of
-    bytes read to bytes written) and torch's 1 : 1 device copy."""
+    bytes read to bytes written) and torch's 1 : 1 device copy.  Beside them,
+    plain torch kernels of the copy-in's and the copy-out's own byte counts
+    and read : write mixes (an FP32 -> BF16 cast, 2 : 1; a byte copy, 1 : 1),
+    which show what one launch of that size reaches on this GPU."""
+    pack_bytes = nbytes["pack"]
     n = pack_bytes // 6 // 8 * 8          # BF16 elements: 2n read + 4n written
     src = [torch.empty(2 * n, dtype=torch.uint8, device="cuda").random_(0, 256) for _ in range(2)]
     dst = [torch.empty(4 * n, dtype=torch.uint8, device="cuda") for _ in range(2)]
@@ -672,11 +676,27 @@ def same_run_references(fp, torch, pack_bytes, iters):
     b = [torch.empty(half, dtype=torch.uint8, device="cuda") for _ in range(2)]
     copy_ms = loop_ms(torch, lambda k: b[k & 1].copy_(a[k & 1]), iters)
     del src, dst, a, b
-    return {"plain_widen_1to2": {"what": "fsdp_debug_stream_widen, BF16 -> FP32, same bytes",
-                                 "bytes": 6 * n, "us": widen_ms * 1e3, "gbs": 6 * n / (widen_ms * 1e-3) / 1e9},
-            "copy_1to1": {"what": "torch copy_ of uint8, half the bytes read and half written",
-                          "bytes": 2 * half, "us": copy_ms * 1e3, "gbs": 2 * half / (copy_ms * 1e-3) / 1e9},
-            "iters": iters}
+    out = {"plain_widen_1to2": {"what": "fsdp_debug_stream_widen, BF16 -> FP32, same bytes",
+                                "bytes": 6 * n, "us": widen_ms * 1e3, "gbs": 6 * n / (widen_ms * 1e-3) / 1e9},
+           "copy_1to1": {"what": "torch copy_ of uint8, half the bytes read and half written",
+                         "bytes": 2 * half, "us": copy_ms * 1e3, "gbs": 2 * half / (copy_ms * 1e-3) / 1e9},
+           "iters": iters}
+    m = nbytes["copy_in"] // 6             # FP32 elements: 4m read + 2m written
+    f = [torch.empty(m, dtype=torch.float32, device="cuda").normal_() for _ in range(2)]
+    g = [torch.empty(m, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    cast_ms = loop_ms(torch, lambda k: g[k & 1].copy_(f[k & 1]), iters)
+    del f, g
+    q = nbytes["copy_out"] // 2 // 16 * 16
+    a = [torch.empty(q, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    b = [torch.empty(q, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    copy_out_ms = loop_ms(torch, lambda k: b[k & 1].copy_(a[k & 1]), iters)
+    del a, b
+    out["copy_in_sized_cast_2to1"] = {"what": "torch FP32 -> BF16 copy_ of the copy-in's byte count",
+                                      "bytes": 6 * m, "us": cast_ms * 1e3, "gbs": 6 * m / (cast_ms * 1e-3) / 1e9}
+    out["copy_out_sized_copy_1to1"] = {"what": "torch copy_ of uint8, the copy-out's byte count",
+                                       "bytes": 2 * q, "us": copy_out_ms * 1e3,
+                                       "gbs": 2 * q / (copy_out_ms * 1e-3) / 1e9}
+    return out
 
 
 def run_packs(fp, groups, h, first, count, batch=None, op="pack"):
@@ -832,7 +852,10 @@ def run_ours(args):
     alone = ops_alone(fp, torch, groups, batch, h, OPS, nbytes, n_launch, args.op_seconds) \
         if args.op_seconds > 0 else None
 
-    refs = same_run_references(fp, torch, nbytes["pack"], args.reference_iters) if args.reference_iters > 0 else None
+    refs = same_run_references(fp, torch, nbytes, args.reference_iters) if args.reference_iters > 0 else None
+    if refs is not None and alone is not None and n_launch == 1:
+        for op, key in (("copy_in", "copy_in_sized_cast_2to1"), ("copy_out", "copy_out_sized_copy_1to1")):
+            alone[op]["same_size_reference_us"] = refs[key]["us"]
     precast = None
     if len(groups) == 1 and args.precast_iters > 0:
         precast = precast_comparison(fp, torch, work, groups[0], h, args.precast_iters, rows)

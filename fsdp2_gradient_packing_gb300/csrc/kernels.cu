@@ -781,6 +781,14 @@ std::atomic<int32_t> g_fault{0};
 std::atomic<int32_t> g_upload_fault{0};  // fsdp_debug_set_upload_fault
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int32_t> g_sched_mode{FSDP_SCHEDULE_DEFAULT};  // fsdp_debug_set_schedule
+std::atomic<int32_t> g_grid_cap{0};                         // fsdp_debug_set_grid_cap
+
+// The grid a table-driven launch actually gets: the planned grid, cut to the
+// test cap when one is set.
+int64_t capped_grid(int64_t grid) {
+  const int64_t cap = g_grid_cap.load(std::memory_order_relaxed);
+  return cap > 0 && grid > cap ? cap : grid;
+}
 
 // A launch shares its last quarter of items when it has at least
 // kSharedMinRounds items per CTA -- a batched launch when its layouts have
@@ -826,7 +834,8 @@ fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptr
   a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   a.fault = g_fault.load(std::memory_order_relaxed);
   a.reserved = 0;
-  a.sched = make_sched(L->d_sched + op, &L->sched_epoch[op], a.n_items, L->op[op].grid);
+  const int64_t grid = capped_grid(L->op[op].grid);
+  a.sched = make_sched(L->d_sched + op, &L->sched_epoch[op], a.n_items, grid);
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
   // Programmatic stream serialization: this launch may be scheduled while the
@@ -836,7 +845,7 @@ fsdp_status_t launch_variant(const fsdp_layout *L, Op op, const void *const *ptr
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)L->op[op].grid);
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -891,7 +900,7 @@ fsdp_status_t batch_launch_variant(const fsdp_layout *const *Ls, int n, Op op, c
   a.fault = g_fault.load(std::memory_order_relaxed);
   for (int k = 0; k < n_ptrs; ++k) a.slot[k] = ptrs[k];
   for (int k = n_ptrs; k < NSLOT; ++k) a.slot[k] = nullptr;
-  const int64_t grid = total < Ls[0]->resident ? total : Ls[0]->resident;
+  const int64_t grid = capped_grid(total < Ls[0]->resident ? total : Ls[0]->resident);
   a.sched = make_sched(Ls[0]->d_sched + op, &Ls[0]->sched_epoch[op], total, grid, groups);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1539,7 +1548,7 @@ fsdp_status_t fsdp_pack_reduce_scatter_noalloc(const fsdp_layout_t *L, const voi
     e = cudaMemcpyAsync(table, L->items.data() + L->op[OP_PACK].first, (size_t)count * sizeof(WorkItem),
                         cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return fail(FSDP_ECUDA, std::string("work table copy: ") + cudaGetErrorString(e));
-  const int64_t grid = count < nd.resident ? count : nd.resident;
+  const int64_t grid = capped_grid(count < nd.resident ? count : nd.resident);
   const void *ptrs[kSlotsLarge];
   for (int p = 0; p < P; ++p) ptrs[p] = grads[p];
   for (int b = 0; b < B; ++b) ptrs[P + b] = bucket_bufs[b];
@@ -1584,6 +1593,13 @@ void fsdp_debug_set_wait_fault(int32_t fault, int64_t wait_limit_ns) {
   g_fault.store(fault, std::memory_order_relaxed);
   g_wait_limit_ns.store(wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kDefaultWaitLimitNs,
                         std::memory_order_relaxed);
+}
+
+fsdp_status_t fsdp_debug_set_grid_cap(int32_t max_blocks) {
+  if (max_blocks < 0) return fail(FSDP_EINVAL, "grid cap must be >= 0, got " + std::to_string(max_blocks));
+  g_grid_cap.store(max_blocks, std::memory_order_relaxed);
+  clear_error();
+  return FSDP_OK;
 }
 
 fsdp_status_t fsdp_debug_set_schedule(int32_t mode) {

@@ -100,6 +100,7 @@ _SIGNATURES = {
     "fsdp_debug_set_wait_fault": (None, [ctypes.c_int32, ctypes.c_int64]),
     "fsdp_debug_set_upload_fault": (None, [ctypes.c_int32]),
     "fsdp_debug_set_schedule": (_ST, [ctypes.c_int32]),
+    "fsdp_debug_set_grid_cap": (_ST, [ctypes.c_int32]),
     "fsdp_debug_stream_widen": (_ST, [_P, ctypes.c_int64, _P, _P]),
     "fsdp_layout_destroy": (None, [_LAYOUT]),
     "fsdp_status_string": (ctypes.c_char_p, [_ST]),
@@ -538,6 +539,12 @@ def fsdp_debug_set_upload_fault(fail_upload: bool) -> None:
 
 def fsdp_debug_set_schedule(mode: int) -> None:
     _check(_lib.fsdp_debug_set_schedule(mode), "fsdp_debug_set_schedule")
+
+
+def fsdp_debug_set_grid_cap(max_blocks: int) -> None:
+    """Run every table-driven launch on at most max_blocks blocks (0: the
+    planned grid); a test hook."""
+    _check(_lib.fsdp_debug_set_grid_cap(max_blocks), "fsdp_debug_set_grid_cap")
 
 
 def fsdp_debug_stream_widen(src, n: int, dst, stream=None) -> None:

@@ -416,6 +416,19 @@ typedef enum {
 fsdp_status_t fsdp_debug_set_schedule(int32_t mode);
 
 /*
+ * Test hook, process-wide, not a step of the method.  While max_blocks > 0,
+ * every table-driven launch (pack, copy-in, copy-out, reduce-scatter copy-out,
+ * their batched forms and the allocation-free pack) runs on at most
+ * max_blocks blocks instead of its planned grid, so that a small layout gives
+ * each block many work items and exercises the per-block paths that
+ * otherwise only full-size groups reach.  Results do not depend on the grid.
+ * 0 restores the planned grids.  Takes effect at the next launch; layouts
+ * planned before are affected too.  Returns FSDP_EINVAL (and changes nothing)
+ * for max_blocks < 0.
+ */
+fsdp_status_t fsdp_debug_set_grid_cap(int32_t max_blocks);
+
+/*
  * Measurement utility, not a step of the method: a plain streaming widen of
  * n BF16 elements to FP32 (each FP32 result is the BF16 bits shifted up by
  * 16, exact), which moves bytes at the reduce-scatter pack's own 1 : 2 mix

@@ -272,3 +272,13 @@ def test_stream_widen_checks_its_arguments_without_launching(fp):
             fp.fsdp_debug_stream_widen(src, n, dst, stream=0)
         assert e.value.status == fp.FSDP_EINVAL and why in str(e.value), (src, n, dst)
 
+
+
+def test_grid_cap_hook_accepts_counts_and_refuses_negative(fp):
+    for cap in (1, 7, 456, 1 << 30, 0):
+        fp.fsdp_debug_set_grid_cap(cap)
+    for bad in (-1, -(1 << 20)):
+        with pytest.raises(fp.FsdpError) as e:
+            fp.fsdp_debug_set_grid_cap(bad)
+        assert e.value.status == fp.FSDP_EINVAL and "grid cap" in str(e.value)
+    fp.fsdp_debug_set_grid_cap(0)

@@ -15,7 +15,9 @@ library.  The cases:
     with no synchronisation between them;
   * a layout of exactly as many work items as the array holds, with a ragged
     last item;
-  * a layout one item too large, refused before anything is launched.
+  * a layout one item too large, refused before anything is launched;
+  * calls on grids cut short by the test hook, so that every block walks
+    many of the array's items.
 This file is named to be collected last.
 """
 import numpy as np
@@ -157,3 +159,23 @@ def test_noalloc_rejects_a_table_beyond_its_scratch(fp):
         with pytest.raises(fp.FsdpError) as e:
             fp.fsdp_pack_reduce_scatter_noalloc(L, [0x1000], [0x2000])
         assert e.value.status == fp.FSDP_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("blocks", [1, 5, 40])
+def test_noalloc_pack_on_few_blocks(fp, blocks):
+    """One layer of the ~500-parameter layout (913 pack items) on 1, 5 and
+    40 blocks: every block walks many of the array's items in the fixed
+    order."""
+    work = wl.transformer_500(W=8, layers=1)
+    specs = work.groups[0]
+    h, g = _inputs(work, specs)
+    _, want = _expected(specs, work.W, h)
+    fp.fsdp_debug_set_grid_cap(blocks)
+    try:
+        with fp.fsdp_plan_layout_host(specs, work.W) as L:
+            out = _buckets(fp, L, 0x5A)
+            fp.fsdp_pack_reduce_scatter_noalloc(L, g, out)
+            torch.cuda.synchronize()
+    finally:
+        fp.fsdp_debug_set_grid_cap(0)
+    _assert_equal_to_oracle(out, want, f"no-alloc pack on {blocks} blocks")
