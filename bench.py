@@ -490,6 +490,7 @@ class DeviceSet:
         hoffs, htot = flat_offsets(h_sizes)
         self.sharded = torch.empty(htot, dtype=torch.uint8, device=dev)
         self.sharded_ptrs = fp.pointer_array([self.sharded.data_ptr() + o for o in hoffs])
+        self.W, self.sharded_offs = W, hoffs
         # The other ranks' rows: what the all-gather would deliver.
         for r in range(W):
             if r == rank_row:
@@ -499,6 +500,13 @@ class DeviceSet:
                                       self.gathered.data_ptr() + r * self.S_ag)
             torch.cuda.synchronize()
             del other
+
+    def spare(self, fp, torch):
+        """Fresh copies of what the copy-in and the reduce-scatter copy-out
+        touch (shards, one all-gather row, row 0 of every bucket, sharded
+        gradients), for loops of those short operations that rotate through
+        more memory than L2 holds."""
+        return SpareSet(fp, torch, self)
 
     def pack(self, fp, L, h):
         fp.fsdp_pack_reduce_scatter(L, self.grad_ptrs, self.bucket_ptrs, h)
@@ -547,6 +555,26 @@ class Group:
                      for _ in range(2)]
 
 
+class SpareSet:
+    """See DeviceSet.spare."""
+
+    def __init__(self, fp, torch, ds):
+        self.shards = ds.shards.clone()
+        self.shard_ptrs = fp.pointer_array([self.shards.data_ptr() + o for o in ds.shard_offs])
+        self.row = torch.empty(ds.S_ag, dtype=torch.uint8, device=ds.shards.device)
+        self.row_ptr = self.row.data_ptr()
+        self.row0 = [b[:b.numel() // ds.W].clone() for b in (ds.reduced or ds.buckets)]
+        self.row0_ptrs = fp.pointer_array(self.row0)
+        self.sharded = torch.empty_like(ds.sharded)
+        self.sharded_ptrs = fp.pointer_array([self.sharded.data_ptr() + o for o in ds.sharded_offs])
+
+    def copy_in(self, fp, L, h):
+        fp.fsdp_allgather_copy_in(L, self.shard_ptrs, self.row_ptr, h)
+
+    def rs_copy_out(self, fp, L, h):
+        fp.fsdp_reduce_scatter_copy_out(L, self.row0_ptrs, self.sharded_ptrs, h)
+
+
 class Batch:
     """The pointer arrays of the batched entry points for both buffer sets."""
 
@@ -562,6 +590,13 @@ class Batch:
                 shards=cat(s.shard_ptrs for s in ss), rows=fp.pointer_array([s.row_ptr for s in ss]),
                 gathered=fp.pointer_array([s.gathered.data_ptr() for s in ss]), full=cat(s.full_ptrs for s in ss),
                 row0=cat(s.row0_ptrs for s in ss), sharded=cat(s.sharded_ptrs for s in ss)))
+
+    @staticmethod
+    def spare_args(fp, spares):
+        """Batched pointer arrays of one SpareSet per group."""
+        cat = lambda arrs: fp.pointer_array([p for a in arrs for p in a])  # noqa: E731
+        return dict(shards=cat(s.shard_ptrs for s in spares), rows=fp.pointer_array([s.row_ptr for s in spares]),
+                    row0=cat(s.row0_ptrs for s in spares), sharded=cat(s.sharded_ptrs for s in spares))
 
     def pack(self, fp, h, k):
         a = self.sets[k]
@@ -682,20 +717,23 @@ def same_run_references(fp, torch, nbytes, iters):
                          "bytes": 2 * half, "us": copy_ms * 1e3, "gbs": 2 * half / (copy_ms * 1e-3) / 1e9},
            "iters": iters}
     m = nbytes["copy_in"] // 6             # FP32 elements: 4m read + 2m written
-    f = [torch.empty(m, dtype=torch.float32, device="cuda").normal_() for _ in range(2)]
-    g = [torch.empty(m, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    cast_ms = loop_ms(torch, lambda k: g[k & 1].copy_(f[k & 1]), iters)
+    R = rotation_count(torch, 6 * m)
+    f = [torch.empty(m, dtype=torch.float32, device="cuda").normal_() for _ in range(R)]
+    g = [torch.empty(m, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    cast_ms = loop_ms(torch, lambda k: g[k % R].copy_(f[k % R]), iters)
     del f, g
     q = nbytes["copy_out"] // 2 // 16 * 16
-    a = [torch.empty(q, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    b = [torch.empty(q, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    copy_out_ms = loop_ms(torch, lambda k: b[k & 1].copy_(a[k & 1]), iters)
+    Q = rotation_count(torch, 2 * q)
+    a = [torch.empty(q, dtype=torch.uint8, device="cuda") for _ in range(Q)]
+    b = [torch.empty(q, dtype=torch.uint8, device="cuda") for _ in range(Q)]
+    copy_out_ms = loop_ms(torch, lambda k: b[k % Q].copy_(a[k % Q]), iters)
     del a, b
     out["copy_in_sized_cast_2to1"] = {"what": "torch FP32 -> BF16 copy_ of the copy-in's byte count",
-                                      "bytes": 6 * m, "us": cast_ms * 1e3, "gbs": 6 * m / (cast_ms * 1e-3) / 1e9}
+                                      "bytes": 6 * m, "us": cast_ms * 1e3, "gbs": 6 * m / (cast_ms * 1e-3) / 1e9,
+                                      "rotating_buffer_sets": R}
     out["copy_out_sized_copy_1to1"] = {"what": "torch copy_ of uint8, the copy-out's byte count",
                                        "bytes": 2 * q, "us": copy_out_ms * 1e3,
-                                       "gbs": 2 * q / (copy_out_ms * 1e-3) / 1e9}
+                                       "gbs": 2 * q / (copy_out_ms * 1e-3) / 1e9, "rotating_buffer_sets": Q}
     return out
 
 
@@ -710,19 +748,54 @@ def run_packs(fp, groups, h, first, count, batch=None, op="pack"):
             getattr(grp.sets[i & 1], op)(fp, grp.L, h)
 
 
+def l2_bytes(torch):
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except (AttributeError, RuntimeError):
+        return 129 << 20
+
+
+def rotation_count(torch, nbytes):
+    """Buffers a back-to-back loop rotates through so that it touches at
+    least three times L2 between two uses of one buffer (at least two)."""
+    return max(2, -(-3 * l2_bytes(torch) // max(1, nbytes)))
+
+
 def ops_alone(fp, torch, groups, batch, h, OPS, nbytes, n_launch, seconds):
-    """Each operation alone: launches of that operation back to back
-    (alternating the buffer sets, no events between them), about `seconds`
-    of each after a short estimate."""
+    """Each operation alone: launches of that operation back to back (no
+    events between them), about `seconds` of each after a short estimate.
+    The pack and the copy-out alternate the two buffer sets, which hold more
+    than L2; the copy-in and the reduce-scatter copy-out rotate through as
+    many spare copies of their inputs and outputs as it takes to touch three
+    times L2, so that no call finds the data of a recent one in L2."""
     out = {}
     for op in OPS:
-        est = loop_ms(torch, lambda k: run_packs(fp, groups, h, k, 1, batch, op), 20)
+        fn, R = (lambda k, op=op: run_packs(fp, groups, h, k, 1, batch, op)), 2
+        spares = None
+        if op in ("copy_in", "rs_copy_out") and 2 * nbytes[op] < 3 * l2_bytes(torch):
+            R = rotation_count(torch, nbytes[op])
+            spares = [[grp.sets[r & 1].spare(fp, torch) for grp in groups] for r in range(R)]
+            if batch is not None:
+                args = [Batch.spare_args(fp, sp) for sp in spares]
+                if op == "copy_in":
+                    fn = lambda k: fp.fsdp_allgather_copy_in_batched(  # noqa: E731
+                        batch.layouts, args[k % R]["shards"], args[k % R]["rows"], h)
+                else:
+                    fn = lambda k: fp.fsdp_reduce_scatter_copy_out_batched(  # noqa: E731
+                        batch.layouts, args[k % R]["row0"], args[k % R]["sharded"], h)
+            else:
+                fn = lambda k, op=op: [getattr(sp, op)(fp, grp.L, h)  # noqa: E731
+                                       for sp, grp in zip(spares[k % R], groups)]
+        est = loop_ms(torch, fn, 20)
         iters = max(50, int(seconds / (est * 1e-3)))
-        ms = loop_ms(torch, lambda k: run_packs(fp, groups, h, k, 1, batch, op), iters)
+        ms = loop_ms(torch, fn, iters)
         out[op] = {"bytes": nbytes[op], "launches_per_call": n_launch, "calls": iters, "us": ms * 1e3,
-                   "gbs": nbytes[op] / (ms * 1e-3) / 1e9}
+                   "gbs": nbytes[op] / (ms * 1e-3) / 1e9, "rotating_buffer_sets": R,
+                   "bytes_between_reuse": R * nbytes[op]}
+        del spares
     for grp in groups:
         fp.fsdp_sync_status(grp.L)
+    torch.cuda.empty_cache()
     return out
 
 
@@ -879,7 +952,9 @@ def run_ours(args):
         if alone is not None:
             result["ops_alone"] = alone
             result["ops_alone_note"] = ("each operation alone, its launches back to back with no events between "
-                                        "them (programmatic dependent launch on): per-call device time")
+                                        "them (programmatic dependent launch on): per-call device time; each loop "
+                                        "rotates through buffer sets that hold more than L2 "
+                                        "(bytes_between_reuse)")
         if precast is not None:
             result["precast_baseline"] = precast
         if extra is not None:

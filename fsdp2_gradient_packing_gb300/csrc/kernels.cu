@@ -34,8 +34,8 @@
 //     reuses it kStages items later.
 // FP32 -> BF16 rounding in walk_kernel is done on the bits (round to nearest,
 // ties to even), so results do not depend on the device's FP modes; the
-// vector path of sum_kernel rounds BF16 pairs with the hardware's
-// round-to-nearest-even conversion, which gives the same bits.
+// vector path of sum_kernel adds BF16 pairs with the hardware's BF16
+// addition (round to nearest even), which gives the same bits.
 //
 // Every mbarrier wait is bounded (a limit in nanoseconds of %globaltimer).  A
 // wait that gives up sets a bit in the layout's device status word and the
@@ -76,11 +76,12 @@ static_assert(kStageDataBytes % 16 == 0, "stage header must stay 16-byte aligned
 constexpr int kPrefetch = 32;
 constexpr int64_t kPrologueMaxRounds = 64;
 // Items per CTA whose staged source is prefetched into L2 before the
-// dependent-launch wait: the ones that fill the ring first, and only in a CTA
-// that has more fixed-order items than that to follow.  Without the parallel
-// prologue the producer looks them up one after another, which pays off only
-// in launches of at least kSeqPrefetchMinRounds items per CTA; shorter ones
-// look up (and prefetch) item 0 alone.
+// dependent-launch wait: the ones that fill the ring first, in a CTA that has
+// more fixed-order items than that to follow.  A CTA whose whole work fits the
+// ring prefetches its first item only.  Without the parallel prologue the
+// producer looks them up one after another, which pays off only in launches
+// of at least kSeqPrefetchMinRounds items per CTA; shorter ones look up (and
+// prefetch) item 0 alone.
 constexpr int kL2PrefetchItems = kStages;
 constexpr int64_t kSeqPrefetchMinRounds = 16;
 constexpr int kMaxBatch = 64;  // layouts in one batched launch
@@ -354,9 +355,10 @@ static_assert(sizeof(StageHeader) == 32, "the prefetch table holds 32-byte heade
 // griddepcontrol.wait still reads whatever that kernel wrote.  Issued by a
 // launch whose blocks start while the previous launch drains, it puts the
 // first reads in flight during that tail instead of after it.  A CTA whose
-// whole work is those first items does not prefetch: when nothing overlaps
-// (a previous kernel that does not release its dependents early), a launch
-// whose every read waits behind its own prefetch was measured slower.
+// whole work fits the ring prefetches its first item only.  Measured on one
+// GB300, prefetching three or four such items made launches slower when
+// nothing overlaps (behind a kernel that does not release its dependents
+// early); the first item alone gained back to back and behind such kernels.
 __device__ __forceinline__ void prefetch_item(const StageHeader &h) {
   const int ss = (h.kind & 1) ? 2 : 4;
   const Staged st = staged_of(h.src, h.n_copy * ss);
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         const WorkItem w = a.fetch(blockIdx.x + (int64_t)lane * G, &base, &cur);
         const StageHeader h = resolve_item(a, w, base);
         pre[lane] = h;
-        if (n_fixed > kStages && lane < kL2PrefetchItems) prefetch_item(h);
+        if (lane < (n_fixed > kStages ? kL2PrefetchItems : 1)) prefetch_item(h);
       }
       __syncwarp();
     }
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
         int32_t base = 0;
         const WorkItem w = a.fetch(blockIdx.x + mi * G, &base, &cursor);
         pre[mi] = resolve_item(a, w, base);
-        if (n_fixed > kStages) prefetch_item(pre[mi]);
+        if (n_fixed > kStages || mi == 0) prefetch_item(pre[mi]);
       }
       n_pre = (int)n_seq;
     }
@@ -958,17 +960,18 @@ __device__ __forceinline__ uint32_t add_bits(uint32_t acc, uint32_t x) {
   }
 }
 
-// Two BF16 sums at once: the two binary32 additions, then one hardware
-// round-to-nearest-even conversion of both sums to a BF16 pair (the same
-// rounding add_bits does with integer operations, in one instruction), then
-// a NaN sum in either half becomes the canonical quiet NaN.
+// Two BF16 sums at once with the hardware's BF16 pair addition, which rounds
+// each exact sum to nearest, ties to even.  That is the same result as
+// add_bits<true>: adding two BF16 values in binary32 and rounding the sum to
+// BF16 rounds twice, but binary32 keeps at least 2 x 8 + 1 significant bits,
+// and with that margin a second rounding of a sum always lands where one
+// rounding of the exact sum does.  A NaN sum in either half becomes the
+// canonical quiet NaN.
 __device__ __forceinline__ uint32_t add_bf16_pair(uint32_t x, uint32_t y) {
-  const float s_lo = __fadd_rn(__uint_as_float(x << 16), __uint_as_float(y << 16));
-  const float s_hi = __fadd_rn(__uint_as_float(x & 0xFFFF0000u), __uint_as_float(y & 0xFFFF0000u));
   uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(s_hi), "f"(s_lo));
-  if (s_lo != s_lo) d = (d & 0xFFFF0000u) | 0x7FC0u;
-  if (s_hi != s_hi) d = (d & 0x0000FFFFu) | 0x7FC00000u;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(y));
+  if ((d & 0x7FFFu) > 0x7F80u) d = (d & 0xFFFF0000u) | 0x7FC0u;
+  if ((d & 0x7FFF0000u) > 0x7F800000u) d = (d & 0x0000FFFFu) | 0x7FC00000u;
   return d;
 }
 

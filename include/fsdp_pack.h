@@ -274,7 +274,8 @@ fsdp_status_t fsdp_reduce_scatter_copy_out(const fsdp_layout_t *L, const void *c
  * ranks q = 0, 1, ..., W-1 in that order with every partial sum rounded to
  * the bucket dtype: FP32, one IEEE binary32 addition rounded to nearest even
  * (subnormals kept); BF16, a binary32 addition of the two values, then round
- * to nearest even to BF16.  A NaN sum (a NaN operand, or infinities of
+ * to nearest even to BF16 (which equals the BF16 value nearest to the exact
+ * sum: binary32 carries more than twice BF16's significant bits).  A NaN sum (a NaN operand, or infinities of
  * opposite sign) is the canonical quiet NaN 0x7FC00000 / 0x7FC0; rank 0's
  * value enters unchanged.  A fixed order makes the result reproducible bit
  * for bit ("Training frameworks" note, "Check the objective before measuring

@@ -659,6 +659,61 @@ def test_emulated_rs_bf16_rounds_every_partial_sum():
     assert _ers(BF16, [np.array([tiny]), np.array([tiny]), np.array([one])])[0] == 0x3F81
 
 
+def _bf16_exact_sum(a: int, b: int) -> int:
+    """The BF16 pattern nearest to the exact sum of the finite BF16 patterns a
+    and b (ties to even): the sum as a Fraction, scaled to the BF16 quantum
+    of its binade and rounded with Python's ties-to-even round()."""
+    val = lambda u: Fraction(*np.uint32(u << 16).view(np.float32).item().as_integer_ratio())  # noqa: E731
+    x = val(a) + val(b)
+    if x == 0:                                 # -0 only from -0 + -0
+        return 0x8000 if (a & 0x8000) and (b & 0x8000) else 0
+    e = abs(x).numerator.bit_length() - abs(x).denominator.bit_length()
+    while Fraction(2) ** e > abs(x):
+        e -= 1
+    while Fraction(2) ** (e + 1) <= abs(x):
+        e += 1
+    q = Fraction(2) ** (max(-126, e) - 7)
+    y = round(x / q) * q
+    if abs(y) >= Fraction(2) ** 128:
+        return 0xFF80 if x < 0 else 0x7F80
+    bits = int(np.float32(float(y)).view(np.uint32))   # exact: y is a BF16 value
+    if y == 0:
+        bits = 0x80000000 if x < 0 else 0
+    return bits >> 16
+
+
+def test_emulated_rs_bf16_add_is_the_exactly_rounded_sum():
+    """Each BF16 addition of the emulated reduce-scatter (binary32 sum, then
+    round to nearest even) gives the BF16 value nearest to the exact sum of
+    its two operands: binary32 keeps at least 2 x 8 + 1 significant bits, so
+    the second rounding never moves a result.  Checked against exact
+    rational rounding on random pairs, pairs a half BF16 step apart (ties
+    and near-ties), every exponent gap from 0 to 40, subnormals and
+    cancellations."""
+    rng = np.random.default_rng(71)
+
+    def finite(n):
+        u = rng.integers(0, 1 << 16, 4 * n, dtype=np.uint64).astype(np.uint32)
+        return u[(u & 0x7F80) != 0x7F80][:n]
+
+    a = finite(3000)
+    b = finite(3000)
+    # half a BF16 step of a, give or take a few units of the partner's last place
+    ea = (a >> 7) & 0xFF
+    half = ((np.maximum(ea, 9) - 8) << 7) | rng.integers(0, 4, a.size).astype(np.uint32)
+    half |= rng.integers(0, 2, a.size).astype(np.uint32) << 15
+    gap = rng.integers(0, 41, a.size).astype(np.uint32)
+    shifted = ((np.maximum(ea, gap + 1) - gap) << 7) | (b & 0x807F)
+    sub = a & 0x807F                           # subnormals (and zeros)
+    cancel = (a ^ 0x8000) + rng.integers(0, 3, a.size).astype(np.uint32)
+    cancel = np.where((cancel & 0x7F80) == 0x7F80, a ^ 0x8000, cancel) & 0xFFFF
+    A = np.concatenate([a, a, a, sub, a, sub]).astype(np.uint16)
+    B = np.concatenate([b, half, shifted, b & 0x807F, cancel, sub[::-1]]).astype(np.uint16)
+    got = _ers(BF16, [A, B])
+    for x, y, g in zip(A.tolist(), B.tolist(), got.tolist()):
+        assert g == _bf16_exact_sum(x, y), (hex(x), hex(y), hex(g))
+
+
 def test_emulated_rs_matches_sequential_float32_and_pack_composition():
     rng = np.random.default_rng(47)
     params = [Param(37, BF16, F32, F32), Param(20, F32, BF16, BF16), Param(64, F32, F32, BF16)]
