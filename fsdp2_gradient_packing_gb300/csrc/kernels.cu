@@ -658,7 +658,8 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     // Without the parallel prologue, the producer resolves the items that fill
     // the ring first (at least item 0: blockIdx.x in every schedule, the grid
     // being at most n) one by one into `pre`, also before waiting for the
-    // previous kernel on the stream, and prefetches their sources.
+    // previous kernel on the stream, and prefetches their sources (item 0's
+    // alone in a CTA whose whole work fits the ring).
     if (n_pre == 0) {
       const int64_t depth = n >= kSeqPrefetchMinRounds * G ? kL2PrefetchItems : 1;
       const int64_t n_seq = n_fixed < depth ? n_fixed : depth;
