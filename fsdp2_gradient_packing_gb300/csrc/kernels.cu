@@ -6,9 +6,11 @@
 // cast(src[k]) : +0 for k < n_total.  The host planner (plan.cpp) emits the
 // runs once per layout, cut into work items of at most kStageBytes of source;
 // one launch per call walks them (walk_kernel), or, for the *_batched calls,
-// one launch walks the tables of up to 64 layouts.  Every launch uses
-// programmatic dependent launch: it may be scheduled while the previous kernel
-// on the stream drains, and waits for it before touching memory.  A separate
+// one launch walks the tables of up to 64 layouts.  Every launch but the
+// allocation-free pack's uses programmatic dependent launch: it may be
+// scheduled while the previous kernel on the stream drains, and waits for it
+// before touching memory; meanwhile it prefetches the sources of its first
+// items into L2, a hint that reads nothing into the CTA.  A separate
 // elementwise kernel (sum_kernel) serves the emulated reduce-scatter.
 //
 // The work is bound by HBM bandwidth, so the kernel is a warp-specialised
