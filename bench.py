@@ -971,7 +971,9 @@ def run_ours(args):
 
 
 # The extra workloads of the default run: (key, workload, batched).
-EXTRA_WORKLOADS = (("transformer500_batched", "transformer500", True), ("kda_block_w64", "kda_w64", False))
+EXTRA_WORKLOADS = (("transformer500_batched", "transformer500", True),
+                   ("transformer500_per_group", "transformer500", False),
+                   ("kda_block_w64", "kda_w64", False))
 
 
 def run_extra(fp, torch, h, wname, batched, gpu_id, seconds=0.5):
