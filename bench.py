@@ -210,12 +210,14 @@ def read_peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the kernel and planner sources with comments and whitespace
-    removed, so that only a change of code invalidates a profile."""
+    """Hash of the sources the table-walking kernel and its planner are built
+    from, with comments and whitespace removed, so that only a change of
+    their code invalidates a profile (reduce.cu, the emulated
+    reduce-scatter, is not among them)."""
     import re
     h = hashlib.sha256()
-    for rel in ("fsdp2_gradient_packing_gb300/csrc/kernels.cu", "fsdp2_gradient_packing_gb300/csrc/layout.h",
-                "fsdp2_gradient_packing_gb300/csrc/plan.cpp"):
+    for rel in ("fsdp2_gradient_packing_gb300/csrc/kernels.cu", "fsdp2_gradient_packing_gb300/csrc/bf16_bits.h",
+                "fsdp2_gradient_packing_gb300/csrc/layout.h", "fsdp2_gradient_packing_gb300/csrc/plan.cpp"):
         with open(os.path.join(ROOT, rel)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)

@@ -109,4 +109,11 @@ void clear_error();
 // Device side (kernels.cu): choose grids and upload the work table.
 fsdp_status_t device_setup(fsdp_layout *L);
 void device_release(fsdp_layout *L);
+
+// Host-side argument checks of the entry points (kernels.cu): the layout has
+// a device table on the current device; p is non-NULL (when bytes > 0) and
+// aligned to `align` bytes.  `what` and `index` name the argument in the
+// error message (index < 0: no index).
+fsdp_status_t check_layout(const fsdp_layout *L);
+fsdp_status_t check_ptr(const void *p, int64_t bytes, int64_t align, const char *what, int64_t index);
 }  // namespace fsdp
