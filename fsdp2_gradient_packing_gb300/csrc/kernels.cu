@@ -570,6 +570,39 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       }
       __syncwarp();
     }
+    // First ring fill, in parallel: after the dependent-launch wait, lane s
+    // stages the CTA's fixed-order item s into stage s itself (header, armed
+    // barrier, bulk copy), so the first copies go out together instead of one
+    // after another from the producer lane.  A CTA that shares its last items
+    // keeps one fixed-order item for the producer's claim loop to start from.
+    int n_first = 0;
+    bool skip0 = false;
+    if (n_pre > 0) {
+      const int64_t avail = sc.word ? n_fixed - 1 : n_fixed;
+      n_first = avail < kStages ? (int)(avail > 0 ? avail : 0) : kStages;
+      if (n_first > 0) {
+        wait_for_previous_grid();
+        if (lane < n_first) {
+          const StageHeader h = pre[lane];
+          if (lane == 0 && blockIdx.x == 0 && (a.fault & kFaultSkipFirstStage)) {
+            skip0 = true;
+          } else {
+            const Staged st = staged_of(h.src, h.n_copy * ((h.kind & 1) ? 2 : 4));
+            uint32_t bytes = (uint32_t)st.bytes;
+            StageHeader *hd = reinterpret_cast<StageHeader *>(smem + lane * kStageStride + kStageDataBytes);
+            *hd = h;
+            if (bytes > (uint32_t)kStagedMax) {  // never planned; the consumers skip it
+              atomicOr(a.status, kStatusBadItem);
+              hd->kind = kSkipItem;
+              bytes = 0;
+            }
+            mbar_arrive_expect_tx(&full[lane], bytes);
+            if (bytes) bulk_copy_g2s(smem + lane * kStageStride, h.src - st.lead, bytes, &full[lane]);
+          }
+        }
+        __syncwarp();
+      }
+    }
     if (lane != 0) return;
     // Producer (lane 0).  Item indices are claimed two items ahead of use,
     // and the descriptors of items past the prefetched ones are fetched one
@@ -615,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       }
       return n;
     };
-    int64_t k = 0;
-    bool skipped_first = false, stopped = false;
+    int64_t k = n_first;  // stages armed so far
+    bool skipped_first = skip0, stopped = false;
     int cursor = 0;  // layout of the last fetched item (batched launches)
     // Stage the item with resolved header h in the ring; false if the stage
     // never came free (the wait gave up).
@@ -670,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       // each descriptor is fetched one item ahead.
       WorkItem nxt{};
       int32_t nxt_base = 0;
-      for (int64_t i = blockIdx.x, mi = 0; i < n; i += G, ++mi) {
+      for (int64_t mi = n_first, i = blockIdx.x + mi * G; i < n; i += G, ++mi) {
         const StageHeader h = mi == 0 ? h0 : mi < n_pre ? pre[mi] : resolve_item(a, nxt, nxt_base);
         if (mi + 1 >= n_pre && i + G < n) nxt = a.fetch(i + G, &nxt_base, &cursor);
         if (!stage_item(h)) {
@@ -685,9 +718,9 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       // header (c0_pm >= 0) or a fetched descriptor (c0_pm == -1).  Joining
       // the word comes after the wait above, when an earlier launch of the
       // same operation on the stream has let go of it.
-      m = 1;
-      int64_t c0 = blockIdx.x;
-      int32_t c0_pm = -2, c0_base = 0;
+      m = 1 + n_first;
+      int64_t c0 = blockIdx.x + n_first * G;
+      int32_t c0_pm = n_first > 0 ? n_first : -2, c0_base = 0;
       WorkItem c0_w{};
       Claim q1{};
       bool primed = false;
