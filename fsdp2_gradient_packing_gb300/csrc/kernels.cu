@@ -570,16 +570,41 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       }
       __syncwarp();
     }
+    // Without the parallel prologue, lane 0 resolves the items that fill the
+    // ring first (at least item 0: blockIdx.x in every schedule, the grid
+    // being at most n) one by one into `pre`, also before waiting for the
+    // previous kernel on the stream, and prefetches their sources (item 0's
+    // alone in a CTA whose whole work fits the ring).
+    int cursor = 0;  // layout of the last fetched item (batched launches; lane 0's walk)
+    if (n_pre == 0) {
+      const int64_t depth = n >= kSeqPrefetchMinRounds * G ? kL2PrefetchItems : 1;
+      const int n_seq = (int)(n_fixed < depth ? n_fixed : depth);
+      if (lane == 0) {
+        for (int mi = 0; mi < n_seq; ++mi) {
+          int32_t base = 0;
+          const WorkItem w = a.fetch(blockIdx.x + (int64_t)mi * G, &base, &cursor);
+          pre[mi] = resolve_item(a, w, base);
+          if (n_fixed > kStages || mi == 0) prefetch_item(pre[mi]);
+        }
+      }
+      __syncwarp();
+      n_pre = n_seq;
+    }
     // First ring fill, in parallel: after the dependent-launch wait, lane s
     // stages the CTA's fixed-order item s into stage s itself (header, armed
     // barrier, bulk copy), so the first copies go out together instead of one
-    // after another from the producer lane.  A CTA that shares its last items
-    // keeps one fixed-order item for the producer's claim loop to start from.
+    // after another from the producer lane.  When more items follow, one
+    // resolved header stays for the producer's loop to start from: a CTA that
+    // shares its last items keeps one fixed-order item for its claim loop,
+    // and one whose later descriptors are fetched one ahead keeps the last
+    // resolved one.
     int n_first = 0;
     bool skip0 = false;
-    if (n_pre > 0) {
+    {
       const int64_t avail = sc.word ? n_fixed - 1 : n_fixed;
-      n_first = avail < kStages ? (int)(avail > 0 ? avail : 0) : kStages;
+      const int64_t keep = sc.word || n_pre < n_fixed ? n_pre - 1 : n_pre;
+      const int64_t nf = avail < keep ? avail : keep;
+      n_first = nf < kStages ? (int)(nf > 0 ? nf : 0) : kStages;
       if (n_first > 0) {
         wait_for_previous_grid();
         if (lane < n_first) {
@@ -650,7 +675,6 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
     };
     int64_t k = n_first;  // stages armed so far
     bool skipped_first = skip0, stopped = false;
-    int cursor = 0;  // layout of the last fetched item (batched launches)
     // Stage the item with resolved header h in the ring; false if the stage
     // never came free (the wait gave up).
     auto stage_item = [&](const StageHeader &h) -> bool {
@@ -680,22 +704,6 @@ __global__ void __launch_bounds__(kThreads, 3) walk_kernel(const __grid_constant
       ++k;
       return true;
     };
-    // Without the parallel prologue, the producer resolves the items that fill
-    // the ring first (at least item 0: blockIdx.x in every schedule, the grid
-    // being at most n) one by one into `pre`, also before waiting for the
-    // previous kernel on the stream, and prefetches their sources (item 0's
-    // alone in a CTA whose whole work fits the ring).
-    if (n_pre == 0) {
-      const int64_t depth = n >= kSeqPrefetchMinRounds * G ? kL2PrefetchItems : 1;
-      const int64_t n_seq = n_fixed < depth ? n_fixed : depth;
-      for (int64_t mi = 0; mi < n_seq; ++mi) {
-        int32_t base = 0;
-        const WorkItem w = a.fetch(blockIdx.x + mi * G, &base, &cursor);
-        pre[mi] = resolve_item(a, w, base);
-        if (n_fixed > kStages || mi == 0) prefetch_item(pre[mi]);
-      }
-      n_pre = (int)n_seq;
-    }
     const StageHeader h0 = pre[0];
     wait_for_previous_grid();
     if (!sc.word) {
