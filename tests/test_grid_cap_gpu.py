@@ -4,7 +4,7 @@ layouts give every block many work items.
 The kernel treats a block's items differently by their number:
 - In a single launch of at most 64 items per block, the producer warp's lanes resolve up to 32 of the block's fixed-order items at once, before the dependent-launch wait, and after it stage the first four themselves (one fewer in a block that shares its last items).
 - A block with more fixed-order items than its 4-stage ring prefetches the first 4 into L2; a block whose whole work fits the ring prefetches its first.
-- Longer launches and batched launches look up their first 1 or 4 items one by one (4 from 16 items per block).
+- Longer launches and batched launches look up their first 1 or 4 items one by one (4 from 16 items per block), and the lanes stage all but the last of them at once.
 - A launch with at least 8 items per block (per layout, when batched) shares its last quarter through the work-sharing word.
 
 At their planned grids, full-size groups reach these paths only at a few
