@@ -721,30 +721,52 @@ def test_nondefault_stream(fp):
         run.close()
 
 
-def test_bounded_wait_reports_timeout_and_recovers(fp):
+@pytest.mark.parametrize("launch", ["single", "single_on_4_blocks", "batched", "batched_on_4_blocks"])
+def test_bounded_wait_reports_timeout_and_recovers(fp, launch):
     """A pipeline stage that is never armed makes its consumers hit the wait
     limit: the kernel returns, fsdp_sync_status reports FSDP_ETIMEOUT, and
-    the next call runs normally.  No fault, no hang."""
-    work = wl.transformer_500(W=8, layers=1)
-    specs = work.groups[0]
-    run = GroupRun(fp, specs, 8, work, 0)
+    the next call runs normally.  No fault, no hang.  The unarmed stage is
+    block 0's first, whichever path stages it: the producer warp's lanes
+    after resolving the block's items in parallel (a single launch), lane 0
+    after resolving 4 items one by one (a single launch with more than 64
+    items per block, on 4 blocks; a batched launch of at least 16 items per
+    block), or the producer lane's own loop (a short batched launch)."""
+    work = wl.transformer_500(W=8, layers=2)
+    runs = [GroupRun(fp, work.groups[g], 8, work, g) for g in range(2)]
+    batched = launch.startswith("batched")
+    use = runs if batched else runs[:1]
     try:
-        grads = [DevBuf(g.nbytes, 0, g) for g in run.grads]
-        out = DevBuf(8 * run.pl.bucket_S[0] * 4)
-        fp.fsdp_debug_set_wait_fault(1, 50_000_000)   # 50 ms
+        grads = [[DevBuf(g.nbytes, 0, g) for g in run.grads] for run in use]
+        outs = [DevBuf(8 * run.pl.bucket_S[0] * 4) for run in use]
+
+        def pack():
+            if batched:
+                fp.fsdp_pack_reduce_scatter_batched([run.L for run in use], [g.ptr for gs in grads for g in gs],
+                                                    [o.ptr for o in outs])
+            else:
+                fp.fsdp_pack_reduce_scatter(use[0].L, [g.ptr for g in grads[0]], [outs[0].ptr])
+
+        if launch.endswith("on_4_blocks"):
+            fp.fsdp_debug_set_grid_cap(4)
         try:
-            fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [out.ptr])
-            with pytest.raises(fp.FsdpError) as e:
-                fp.fsdp_sync_status(run.L)
-            assert e.value.status == fp.FSDP_ETIMEOUT
+            fp.fsdp_debug_set_wait_fault(1, 50_000_000)   # 50 ms
+            try:
+                pack()
+                with pytest.raises(fp.FsdpError) as e:
+                    fp.fsdp_sync_status(use[0].L)
+                assert e.value.status == fp.FSDP_ETIMEOUT
+            finally:
+                fp.fsdp_debug_set_wait_fault(0, 0)
+            pack()
+            fp.fsdp_sync_status(use[0].L)
         finally:
-            fp.fsdp_debug_set_wait_fault(0, 0)
-        fp.fsdp_pack_reduce_scatter(run.L, [g.ptr for g in grads], [out.ptr])
-        fp.fsdp_sync_status(run.L)
-        assert np.array_equal(out.read(np.uint32), run.pack_expected()[0])
-        assert out.guards_ok()
+            fp.fsdp_debug_set_grid_cap(0)
+        for run, out in zip(use, outs):
+            assert np.array_equal(out.read(np.uint32), run.pack_expected()[0])
+            assert out.guards_ok()
     finally:
-        run.close()
+        for run in runs:
+            run.close()
 
 
 def test_device_table_allocation_failure_reports_enomem(fp):
