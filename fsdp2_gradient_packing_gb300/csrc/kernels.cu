@@ -19,11 +19,12 @@
 // to write only full, aligned 16-byte vectors:
 //   * warp 0, lane 0 is the producer (in short single launches the warp's
 //     lanes first resolve the CTA's first items -- descriptor and source /
-//     destination pointers -- in parallel, one per lane).  For each item of
-//     its CTA the producer copies the item's source bytes, widened to whole
-//     aligned 16-byte blocks, into one stage of a shared-memory ring with one
-//     TMA bulk copy (cp.async.bulk), completion counted on that stage's
-//     "full" mbarrier;
+//     destination pointers -- in parallel, one per lane, and the lanes
+//     stage the ring's first fill together).  For each item of its CTA the
+//     producer copies the item's source bytes, widened to whole aligned
+//     16-byte blocks, into one stage of a shared-memory ring with one TMA
+//     bulk copy (cp.async.bulk), completion counted on that stage's "full"
+//     mbarrier;
 //   * warps 1..8 are consumers.  For each item they wait on the stage, then
 //     write the destination as 16-byte vectors: each lane reads the source
 //     bytes of one vector from shared memory at whatever byte phase they have
