@@ -51,22 +51,38 @@ __device__ __forceinline__ uint32_t add_bits(uint32_t acc, uint32_t x) {
 // add_bits<true>: adding two BF16 values in binary32 and rounding the sum to
 // BF16 rounds twice, but binary32 keeps at least 2 x 8 + 1 significant bits,
 // and with that margin a second rounding of a sum always lands where one
-// rounding of the exact sum does.  A NaN sum in either half becomes the
-// canonical quiet NaN.
-__device__ __forceinline__ uint32_t add_bf16_pair(uint32_t x, uint32_t y) {
+// rounding of the exact sum does.  NaN sums keep the hardware's payload here;
+// canonical_nan_pair makes them the canonical quiet NaN.
+__device__ __forceinline__ uint32_t add_bf16_raw(uint32_t x, uint32_t y) {
   uint32_t d;
   asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(y));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t canonical_nan_pair(uint32_t d) {
   if ((d & 0x7FFFu) > 0x7F80u) d = (d & 0xFFFF0000u) | 0x7FC0u;
   if ((d & 0x7FFF0000u) > 0x7F800000u) d = (d & 0x0000FFFFu) | 0x7FC00000u;
   return d;
 }
 
-// Lane-wise sum of two 16-byte vectors of elements.
+// Bit 15 or 31 set where that half of d is a NaN: a half h (sign dropped)
+// is a NaN when h > 0x7F80, i.e. when h + 0x7F carries into bit 15.  The
+// sum stays below 0x10000, so nothing carries into the other half.
+__device__ __forceinline__ uint32_t nan_halves(uint32_t d) {
+  return ((d & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u;
+}
+
+// Lane-wise sum of two 16-byte vectors of elements.  For BF16 the NaN
+// fix-up runs only when one of the eight sums is a NaN.
 template <bool BF16>
 __device__ __forceinline__ uint4 add_vec(uint4 a, uint4 b) {
   if constexpr (BF16) {
-    return make_uint4(add_bf16_pair(a.x, b.x), add_bf16_pair(a.y, b.y), add_bf16_pair(a.z, b.z),
-                      add_bf16_pair(a.w, b.w));
+    uint4 d = make_uint4(add_bf16_raw(a.x, b.x), add_bf16_raw(a.y, b.y), add_bf16_raw(a.z, b.z),
+                         add_bf16_raw(a.w, b.w));
+    if (nan_halves(d.x) | nan_halves(d.y) | nan_halves(d.z) | nan_halves(d.w))
+      d = make_uint4(canonical_nan_pair(d.x), canonical_nan_pair(d.y), canonical_nan_pair(d.z),
+                     canonical_nan_pair(d.w));
+    return d;
   } else {
     return make_uint4(add_bits<false>(a.x, b.x), add_bits<false>(a.y, b.y), add_bits<false>(a.z, b.z),
                       add_bits<false>(a.w, b.w));
