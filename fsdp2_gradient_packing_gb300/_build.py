@@ -44,10 +44,21 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link the library if it is missing or stale; return its path."""
+    """Compile and link the library if it is missing or stale; return its path.
+    Processes that call this at once (the ranks of one job) take turns on a
+    lock file, so only the first builds and the others find it fresh."""
     if not force and not _stale():
         return LIB
+    import fcntl
     os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _stale():
+            return LIB
+        return _build_locked(verbose, ptxas_info)
+
+
+def _build_locked(verbose: bool, ptxas_info: bool) -> str:
     cuda = _cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
     objs, procs = [], []
